@@ -1,0 +1,220 @@
+/*
+ * stv.h -- C ABI of the GB300 (sm_103a) tree-verify library: one speculative
+ * decoding verify round over a paged 3-bit KV cache.
+ *
+ * What the round computes (page titles and sections it follows):
+ *  - "elpis" README, header table: the target keeps a 3-bit KV cache
+ *    (12 KiB per token over 16 attention layers) with a 262,144-token native
+ *    context.  -> stv_kv_append_pack
+ *  - "elpis" README, "Why fast" table: a draft proposes 7 tokens arranged as
+ *    an 8-row token tree; the target verifies all rows in one pass (decode
+ *    verify with the 3-bit K codes used as exact int8 values against int8 Q);
+ *    the engine commits the longest matching path + 1.
+ *    -> stv_verify_attn (STV_PATH_EXACT / STV_PATH_INT8), stv_tree_accept,
+ *       stv_kv_commit
+ *  - Reddit posts (u/iamMess), second post: the verify step needs split-KV
+ *    attention because a few query rows alone cannot fill the GPU.
+ *    -> stv_verify_attn writes per-split partials, stv_split_combine merges them
+ *  - "elpis" README, "Why fast": host check after launch (tree verify pipe).
+ *    -> nothing here synchronises; acceptance and commit stay on the device.
+ *  - syv-ai README (mirror), split-KV scratch buffer section: the verify
+ *    workspace must be sized and owned by someone.
+ *    -> stv_verify_workspace_bytes; the caller owns the workspace.
+ *
+ * Conventions (every entry point):
+ *  - extern "C"; returns STV_OK (0) or a negative STV_ERR_* status.  Host
+ *    arguments are validated before anything is enqueued; on a negative
+ *    status nothing was enqueued.
+ *  - Pointers documented "device" are caller-owned device memory; the library
+ *    never allocates, frees or synchronises, and keeps no pointer after the
+ *    call returns.  All work is enqueued on `stream` (NULL = legacy default
+ *    stream); asynchronous CUDA faults surface at the caller's next sync.
+ *  - Data that lives on the device (page tables, row positions, parent
+ *    arrays, commit counts) cannot be checked on the host.  Kernels check it
+ *    as they read it, never touch memory outside the described buffers, and
+ *    OR an STV_DEV_* bit into *dev_status (device int32, may be NULL).
+ *  - Supported shape: head_dim 256, group 32, page_tokens 256, hq = G * hkv
+ *    with T * G <= 128 query rows per KV head, 1 <= T <= 32 tree nodes,
+ *    1 <= n_seqs <= STV_MAX_SEQS.
+ *
+ * Paged cache layout (one pool per layer; page_bytes = hkv * 57,344 for the
+ * supported shape).  Inside a page, KV head h owns the block at h * 57,344:
+ *    [0, 24576)      K codes   [256 tokens][8 groups][3 x uint32]
+ *    [24576, 28672)  K scales  [256 tokens][8 groups] fp16
+ *    [28672, 53248)  V codes   [4 tiles of 64 tokens][256 channels][2 blocks][3 x uint32]
+ *    [53248, 57344)  V scales  [4 tiles][8 groups][64 tokens] fp16
+ * Quantizer, per (token, KV head, group of 32 channels), for K and V alike:
+ * s = fp16(max|x| / 4); code c = clamp(rne(x / s) + 4, 0, 7) (round half to
+ * even; all codes 4 when s == 0); decoded value s * (c - 4).  A block of 32
+ * codes (32 channels of one token for K, 32 tokens of one channel for V) is
+ * three little-endian uint32 W0..W2: for j in 0..2, k in 0..4, m = 5j + k,
+ * code 2m sits in bits 3k..3k+2 of Wj and code 2m+1 in bits 16+3k..16+3k+2
+ * of Wj; bit b of code 30 is bit 15 of Wb, bit b of code 31 is bit 31 of Wb.
+ */
+#ifndef STV_H_
+#define STV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* stv_stream_t;
+
+#define STV_MAX_SEQS 64
+#define STV_HEAD_DIM 256
+#define STV_GROUP 32
+#define STV_PAGE_TOKENS 256
+#define STV_HEAD_BLOCK_BYTES 57344
+
+enum stv_status {
+  STV_OK = 0,
+  STV_ERR_INVALID_ARG = -1,         /* null pointer, negative count, bad enum */
+  STV_ERR_SHAPE_UNSUPPORTED = -2,   /* shape outside the supported set */
+  STV_ERR_WORKSPACE_TOO_SMALL = -3, /* ws_bytes below stv_verify_workspace_bytes */
+  STV_ERR_CUDA = -4,                /* a CUDA runtime call or launch failed */
+  STV_ERR_UNIMPLEMENTED = -5,
+};
+
+/* Bits OR-ed into *dev_status by kernels that find bad device-side data. */
+enum stv_dev_status {
+  STV_DEV_BAD_PAGE = 1,   /* page-table entry outside the pool, or position past the table */
+  STV_DEV_BAD_TREE = 2,   /* parent[0] != -1 or parent[i] outside [0, i) */
+  STV_DEV_BAD_ROW = 4,    /* row_seq outside [0, n_seqs) or row_pos negative */
+  STV_DEV_BAD_COMMIT = 8, /* n_commit outside [1, T] or path not a root path */
+};
+
+enum stv_path { STV_PATH_EXACT = 0, STV_PATH_INT8 = 1 };
+
+typedef struct {
+  int32_t hq;          /* query heads (24 for the pages' model) */
+  int32_t hkv;         /* KV heads (4) */
+  int32_t head_dim;    /* must be 256 */
+  int32_t group;       /* quantization group, must be 32 */
+  int32_t page_tokens; /* must be 256 */
+} stv_shape;
+
+typedef struct {
+  uint8_t* pool;      /* device: n_pages * page_bytes bytes */
+  int64_t page_bytes; /* must equal hkv * STV_HEAD_BLOCK_BYTES */
+  int32_t n_pages;
+} stv_layer_cache;
+
+typedef struct {
+  const int32_t* page_table; /* device: n_pages entries, each in [0, pool n_pages) */
+  int32_t n_pages;           /* logical pages of this sequence */
+  int32_t ctx;               /* cached tokens before this round's tree rows */
+} stv_seq;
+
+/* Name of a status code (static string). */
+const char* stv_status_string(int status);
+
+/* Library ABI version (monotonic). */
+int stv_version(void);
+
+/* Bytes of one page for `shape` (hkv * 57,344). */
+int stv_page_bytes(const stv_shape* shape, int64_t* bytes);
+
+/*
+ * a1 -- quantize fp16 K/V rows into the paged 3-bit cache ("elpis" README,
+ * header table: 3-bit KV cache).
+ *  k, v:      device fp16 [n_rows][hkv][256].
+ *  row_seq:   device int32 [n_rows], sequence of each row.
+ *  row_pos:   device int32 [n_rows], token position of each row in its
+ *             sequence; page row_pos / 256 of that sequence's table, slot
+ *             row_pos % 256.  Two rows may not share a (sequence, position).
+ * A verify round appends its T tree rows at ctx .. ctx + T - 1.
+ */
+int stv_kv_append_pack(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs, int n_seqs,
+                       const void* k, const void* v, const int32_t* row_seq, const int32_t* row_pos, int n_rows,
+                       int32_t* dev_status, stv_stream_t stream);
+
+/*
+ * Workspace for stv_verify_attn / stv_split_combine: per-split partial
+ * outputs (fp32), their row maxima and sums, the int8 Q rows and scales.
+ * sm_count: SMs the split plan targets; 0 = the current device's count
+ * (stv_verify_attn and stv_split_combine always plan for the current device).
+ */
+int stv_verify_workspace_bytes(const stv_shape* shape, const stv_seq* seqs, int n_seqs, int t_nodes, int sm_count,
+                               size_t* bytes);
+
+/*
+ * a2..a4 -- tree-masked split-KV GQA attention of the round's T nodes over
+ * every cached token ("elpis" README, "Why fast": 8-row token tree, decode
+ * verify; Reddit posts, second post: split-KV verify attention).
+ *  q:       device fp16 [n_seqs][T][hq][256] (node-major, then Q head).
+ *  parent:  device int32 [n_seqs][T], parent[0] = -1, parent[i] in [0, i).
+ *  path:    STV_PATH_EXACT: Q fp16 times K dequantized to fp16, fp32 sums;
+ *           STV_PATH_INT8: Q quantized per row to int8 (qi = rne(127 q /
+ *           max|q|)) times the 3-bit K codes, scaled per group.
+ * Key j < ctx is visible to every node; key ctx + k is visible to node i iff
+ * k is i or an ancestor of i.  Scores are q . k / 16; softmax in fp32; P is
+ * rounded to fp16 and P . V accumulates in fp32.  Writes partials into the
+ * workspace; stv_split_combine produces the output.  The round's tree rows
+ * must already be in the cache (stv_kv_append_pack).
+ */
+int stv_verify_attn(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs, int n_seqs,
+                    const void* q, const int32_t* parent, int t_nodes, int path, void* workspace, size_t ws_bytes,
+                    int32_t* dev_status, stv_stream_t stream);
+
+/*
+ * a5 -- merge the split partials of the last stv_verify_attn on this
+ * workspace: per row M = max_s m_s, O = sum_s 2^(m_s - M) O_s / sum_s
+ * 2^(m_s - M) l_s, splits taken in a fixed order (deterministic).
+ *  o: device fp16 [n_seqs][T][hq][256].
+ */
+int stv_split_combine(const stv_shape* shape, const stv_seq* seqs, int n_seqs, int t_nodes, const void* workspace,
+                      size_t ws_bytes, void* o, stv_stream_t stream);
+
+/*
+ * a6 -- exact greedy tree acceptance ("elpis" README, "Why fast": commit the
+ * longest matching path + 1; "elpis-lossless" README, "Lossless": token ids
+ * compared exactly).  Edge p -> c matches iff draft_ids[c] ==
+ * target_argmax[p].  Longest root path of matching edges; among equally
+ * long ones the lexicographically smallest node-index sequence.
+ *  parent, draft_ids, target_argmax: device int32 [n_seqs][T].
+ *  n_commit: device int32 [n_seqs] = accepted depth + 1 (0 for a bad tree).
+ *  path:     device int32 [n_seqs][T], first n_commit entries: node indices
+ *            from the root (path[0] = 0); the rest are set to -1.
+ *  out_ids:  device int32 [n_seqs][T], first n_commit entries: the accepted
+ *            drafts, then the bonus token target_argmax[last node]; rest -1.
+ */
+int stv_tree_accept(const int32_t* parent, const int32_t* draft_ids, const int32_t* target_argmax, int t_nodes,
+                    int n_seqs, int32_t* n_commit, int32_t* path, int32_t* out_ids, int32_t* dev_status,
+                    stv_stream_t stream);
+
+/*
+ * a7 -- compact the accepted rows: for every layer, KV head and i <
+ * n_commit[s], the packed row at slot ctx + path[i] moves to slot ctx + i
+ * (all sources are read before any destination is written), then
+ * ctx_dev[s] += n_commit[s].  Sequences whose n_commit is outside [1, T]
+ * are left untouched (STV_DEV_BAD_COMMIT).
+ *  layers:   host array of n_layers caches (device pools).
+ *  n_commit, path: device, as written by stv_tree_accept.
+ *  ctx_dev:  device int32 [n_seqs] (may be NULL).
+ * Uses seqs[s].ctx (host) as the round's context length.
+ */
+int stv_kv_commit(const stv_shape* shape, const stv_layer_cache* layers, int n_layers, const stv_seq* seqs,
+                  int n_seqs, int t_nodes, const int32_t* n_commit, const int32_t* path, int32_t* ctx_dev,
+                  int32_t* dev_status, stv_stream_t stream);
+
+/*
+ * Inspection entry point for the int8 path ("elpis" README, "Why fast":
+ * 3-bit K codes as exact int8): the exact integer per-group dots
+ * I_g = sum_{c in g} qi_c * (code_c - 4) of one Q row against keys
+ * [tok_begin, tok_end) of one sequence, using the same int8 Q quantizer and
+ * code decoding as STV_PATH_INT8.
+ *  q_row: device fp16 [256]; dots: device int32 [tok_end - tok_begin][8].
+ */
+int stv_int8_qk_dots(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seq, const void* q_row,
+                     int q_head, int32_t tok_begin, int32_t tok_end, int32_t* dots, int32_t* dev_status,
+                     stv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STV_H_ */

@@ -1,0 +1,317 @@
+// api.cu -- the extern "C" entry points of include/stv.h: host-side
+// validation, the split plan, workspace carve-up and kernel launches.  No
+// entry point allocates, frees or synchronises.
+#include <string.h>
+
+#include "stv_internal.h"
+
+namespace stv {
+
+static int check_shape(const stv_shape* sh, int t_nodes, ShapeInfo* out) {
+  if (!sh) return STV_ERR_INVALID_ARG;
+  if (sh->head_dim != kHeadDim || sh->group != kGroup || sh->page_tokens != kPageTok) return STV_ERR_SHAPE_UNSUPPORTED;
+  if (sh->hkv < 1 || sh->hq < sh->hkv || sh->hq % sh->hkv != 0) return STV_ERR_SHAPE_UNSUPPORTED;
+  const int G = sh->hq / sh->hkv;
+  if (t_nodes >= 0) {
+    if (t_nodes < 1 || t_nodes > kMaxT) return STV_ERR_SHAPE_UNSUPPORTED;
+    if (t_nodes * G > kMaxRows) return STV_ERR_SHAPE_UNSUPPORTED;
+  }
+  if (out) {
+    out->hq = sh->hq;
+    out->hkv = sh->hkv;
+    out->G = G;
+    out->T = t_nodes;
+    out->R = t_nodes * G;
+  }
+  return STV_OK;
+}
+
+static int check_layer(const stv_layer_cache* l, int hkv) {
+  if (!l || !l->pool || l->n_pages < 1) return STV_ERR_INVALID_ARG;
+  if (l->page_bytes != (int64_t)hkv * kHeadBytes) return STV_ERR_SHAPE_UNSUPPORTED;
+  return STV_OK;
+}
+
+// need_keys < 0: only the table pointer is checked (append: positions are on
+// the device); otherwise ctx + need_keys must fit in the sequence's pages.
+static int check_seqs(const stv_seq* seqs, int n_seqs, int need_keys) {
+  if (!seqs || n_seqs < 1 || n_seqs > STV_MAX_SEQS) return STV_ERR_INVALID_ARG;
+  for (int s = 0; s < n_seqs; ++s) {
+    if (!seqs[s].page_table || seqs[s].n_pages < 0 || seqs[s].ctx < 0) return STV_ERR_INVALID_ARG;
+    if (need_keys >= 0 && (int64_t)seqs[s].ctx + need_keys > (int64_t)seqs[s].n_pages * kPageTok)
+      return STV_ERR_INVALID_ARG;
+  }
+  return STV_OK;
+}
+
+static int device_sm_count(int* n) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return STV_ERR_CUDA;
+  if (cudaDeviceGetAttribute(n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return STV_ERR_CUDA;
+  return STV_OK;
+}
+
+int make_plan(const ShapeInfo& sh, const stv_seq* seqs, int n_seqs, int sm_count, Plan* plan) {
+  int64_t tiles[STV_MAX_SEQS], total = 0;
+  for (int s = 0; s < n_seqs; ++s) {
+    tiles[s] = ((int64_t)seqs[s].ctx + sh.T + kTileTok - 1) / kTileTok;
+    total += tiles[s] * sh.hkv;
+  }
+  const int64_t target = sm_count > 0 ? sm_count : 1;
+  int64_t k = (total + target - 1) / target;
+  if (k < 1) k = 1;
+  for (;;) {
+    int64_t units = 0;
+    for (int s = 0; s < n_seqs; ++s) units += sh.hkv * ((tiles[s] + k - 1) / k);
+    if (units <= target || units <= (int64_t)n_seqs * sh.hkv) break;
+    ++k;
+  }
+  plan->tiles_per_split = (int)k;
+  int base = 0;
+  for (int s = 0; s < n_seqs; ++s) {
+    plan->splits[s] = (int)((tiles[s] + k - 1) / k);
+    plan->unit_base[s] = base;
+    base += sh.hkv * plan->splits[s];
+  }
+  plan->unit_base[n_seqs] = base;
+  plan->n_units = base;
+  return STV_OK;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+WsLayout ws_layout(const ShapeInfo& sh, int n_seqs, const Plan& plan) {
+  WsLayout w;
+  const size_t q_rows = (size_t)n_seqs * sh.T * sh.hq;
+  size_t at = 0;
+  w.off_qi = at;
+  at = align256(at + q_rows * kHeadDim);
+  w.off_sq = at;
+  at = align256(at + q_rows * sizeof(float));
+  w.off_opart = at;
+  at = align256(at + (size_t)plan.n_units * sh.R * kHeadDim * sizeof(float));
+  w.off_ml = at;
+  at = align256(at + (size_t)plan.n_units * sh.R * 2 * sizeof(float));
+  w.total = at;
+  return w;
+}
+
+static void fill_seq_descs(SeqDesc* out, const stv_seq* seqs, int n_seqs, const Plan* plan) {
+  for (int s = 0; s < n_seqs; ++s) {
+    out[s].page_table = seqs[s].page_table;
+    out[s].n_pages = seqs[s].n_pages;
+    out[s].ctx = seqs[s].ctx;
+    out[s].splits = plan ? plan->splits[s] : 0;
+    out[s].unit_base = plan ? plan->unit_base[s] : 0;
+  }
+}
+
+static int to_status(cudaError_t e) { return e == cudaSuccess ? STV_OK : STV_ERR_CUDA; }
+
+}  // namespace stv
+
+using namespace stv;
+
+extern "C" {
+
+const char* stv_status_string(int status) {
+  switch (status) {
+    case STV_OK: return "STV_OK";
+    case STV_ERR_INVALID_ARG: return "STV_ERR_INVALID_ARG";
+    case STV_ERR_SHAPE_UNSUPPORTED: return "STV_ERR_SHAPE_UNSUPPORTED";
+    case STV_ERR_WORKSPACE_TOO_SMALL: return "STV_ERR_WORKSPACE_TOO_SMALL";
+    case STV_ERR_CUDA: return "STV_ERR_CUDA";
+    case STV_ERR_UNIMPLEMENTED: return "STV_ERR_UNIMPLEMENTED";
+    default: return "STV_ERR_UNKNOWN";
+  }
+}
+
+int stv_version(void) { return 1; }
+
+int stv_page_bytes(const stv_shape* shape, int64_t* bytes) {
+  int rc = check_shape(shape, -1, nullptr);
+  if (rc) return rc;
+  if (!bytes) return STV_ERR_INVALID_ARG;
+  *bytes = (int64_t)shape->hkv * kHeadBytes;
+  return STV_OK;
+}
+
+int stv_kv_append_pack(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs, int n_seqs,
+                       const void* k, const void* v, const int32_t* row_seq, const int32_t* row_pos, int n_rows,
+                       int32_t* dev_status, stv_stream_t stream) {
+  ShapeInfo sh;
+  int rc = check_shape(shape, -1, &sh);
+  if (rc) return rc;
+  if ((rc = check_layer(layer, sh.hkv)) || (rc = check_seqs(seqs, n_seqs, -1))) return rc;
+  if (n_rows < 0 || (n_rows > 0 && (!k || !v || !row_seq || !row_pos))) return STV_ERR_INVALID_ARG;
+  if (n_rows == 0) return STV_OK;
+  AppendParams p;
+  memset(&p, 0, sizeof(p));
+  fill_seq_descs(p.seq, seqs, n_seqs, nullptr);
+  p.n_seqs = n_seqs;
+  p.hkv = sh.hkv;
+  p.pool = layer->pool;
+  p.page_bytes = layer->page_bytes;
+  p.pool_pages = layer->n_pages;
+  p.k = static_cast<const __half*>(k);
+  p.v = static_cast<const __half*>(v);
+  p.row_seq = row_seq;
+  p.row_pos = row_pos;
+  p.n_rows = n_rows;
+  p.status = dev_status;
+  return to_status(launch_kv_append(p, (cudaStream_t)stream));
+}
+
+int stv_verify_workspace_bytes(const stv_shape* shape, const stv_seq* seqs, int n_seqs, int t_nodes, int sm_count,
+                               size_t* bytes) {
+  ShapeInfo sh;
+  int rc = check_shape(shape, t_nodes, &sh);
+  if (rc) return rc;
+  if ((rc = check_seqs(seqs, n_seqs, t_nodes))) return rc;
+  if (!bytes || sm_count < 0) return STV_ERR_INVALID_ARG;
+  if (sm_count == 0 && (rc = device_sm_count(&sm_count))) return rc;
+  Plan plan;
+  make_plan(sh, seqs, n_seqs, sm_count, &plan);
+  *bytes = ws_layout(sh, n_seqs, plan).total;
+  return STV_OK;
+}
+
+int stv_verify_attn(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs, int n_seqs,
+                    const void* q, const int32_t* parent, int t_nodes, int path, void* workspace, size_t ws_bytes,
+                    int32_t* dev_status, stv_stream_t stream) {
+  ShapeInfo sh;
+  int rc = check_shape(shape, t_nodes, &sh);
+  if (rc) return rc;
+  if ((rc = check_layer(layer, sh.hkv)) || (rc = check_seqs(seqs, n_seqs, t_nodes))) return rc;
+  if (!q || !parent || !workspace || (path != STV_PATH_EXACT && path != STV_PATH_INT8)) return STV_ERR_INVALID_ARG;
+  int sm = 0;
+  if ((rc = device_sm_count(&sm))) return rc;
+  Plan plan;
+  make_plan(sh, seqs, n_seqs, sm, &plan);
+  const WsLayout wl = ws_layout(sh, n_seqs, plan);
+  if (ws_bytes < wl.total) return STV_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  VerifyParams p;
+  memset(&p, 0, sizeof(p));
+  fill_seq_descs(p.seq, seqs, n_seqs, &plan);
+  p.n_seqs = n_seqs;
+  p.T = sh.T;
+  p.hq = sh.hq;
+  p.hkv = sh.hkv;
+  p.G = sh.G;
+  p.R = sh.R;
+  p.tiles_per_split = plan.tiles_per_split;
+  p.n_units = plan.n_units;
+  p.path = path;
+  p.pool = layer->pool;
+  p.page_bytes = layer->page_bytes;
+  p.pool_pages = layer->n_pages;
+  p.q = static_cast<const __half*>(q);
+  p.parent = parent;
+  p.qi = reinterpret_cast<const int8_t*>(ws + wl.off_qi);
+  p.sq = reinterpret_cast<const float*>(ws + wl.off_sq);
+  p.o_part = reinterpret_cast<float*>(ws + wl.off_opart);
+  p.ml = reinterpret_cast<float*>(ws + wl.off_ml);
+  p.status = dev_status;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (path == STV_PATH_INT8) {
+    cudaError_t e = launch_quantize_q(p.q, n_seqs * sh.T * sh.hq, reinterpret_cast<int8_t*>(ws + wl.off_qi),
+                                      reinterpret_cast<float*>(ws + wl.off_sq), s);
+    if (e != cudaSuccess) return STV_ERR_CUDA;
+  }
+  return to_status(launch_verify(p, s));
+}
+
+int stv_split_combine(const stv_shape* shape, const stv_seq* seqs, int n_seqs, int t_nodes, const void* workspace,
+                      size_t ws_bytes, void* o, stv_stream_t stream) {
+  ShapeInfo sh;
+  int rc = check_shape(shape, t_nodes, &sh);
+  if (rc) return rc;
+  if ((rc = check_seqs(seqs, n_seqs, t_nodes))) return rc;
+  if (!workspace || !o) return STV_ERR_INVALID_ARG;
+  int sm = 0;
+  if ((rc = device_sm_count(&sm))) return rc;
+  Plan plan;
+  make_plan(sh, seqs, n_seqs, sm, &plan);
+  const WsLayout wl = ws_layout(sh, n_seqs, plan);
+  if (ws_bytes < wl.total) return STV_ERR_WORKSPACE_TOO_SMALL;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  CombineParams p;
+  memset(&p, 0, sizeof(p));
+  fill_seq_descs(p.seq, seqs, n_seqs, &plan);
+  p.n_seqs = n_seqs;
+  p.T = sh.T;
+  p.hq = sh.hq;
+  p.hkv = sh.hkv;
+  p.G = sh.G;
+  p.R = sh.R;
+  p.o_part = reinterpret_cast<const float*>(ws + wl.off_opart);
+  p.ml = reinterpret_cast<const float*>(ws + wl.off_ml);
+  p.o = static_cast<__half*>(o);
+  return to_status(launch_split_combine(p, (cudaStream_t)stream));
+}
+
+int stv_tree_accept(const int32_t* parent, const int32_t* draft_ids, const int32_t* target_argmax, int t_nodes,
+                    int n_seqs, int32_t* n_commit, int32_t* path, int32_t* out_ids, int32_t* dev_status,
+                    stv_stream_t stream) {
+  if (!parent || !draft_ids || !target_argmax || !n_commit || !path || !out_ids) return STV_ERR_INVALID_ARG;
+  if (n_seqs < 1) return STV_ERR_INVALID_ARG;
+  if (t_nodes < 1 || t_nodes > kMaxT) return STV_ERR_SHAPE_UNSUPPORTED;
+  return to_status(launch_tree_accept(parent, draft_ids, target_argmax, t_nodes, n_seqs, n_commit, path, out_ids,
+                                      dev_status, (cudaStream_t)stream));
+}
+
+int stv_kv_commit(const stv_shape* shape, const stv_layer_cache* layers, int n_layers, const stv_seq* seqs,
+                  int n_seqs, int t_nodes, const int32_t* n_commit, const int32_t* path, int32_t* ctx_dev,
+                  int32_t* dev_status, stv_stream_t stream) {
+  ShapeInfo sh;
+  int rc = check_shape(shape, t_nodes, &sh);
+  if (rc) return rc;
+  if (!layers || n_layers < 1 || n_layers > kMaxLayers || !n_commit || !path) return STV_ERR_INVALID_ARG;
+  if ((rc = check_seqs(seqs, n_seqs, t_nodes))) return rc;
+  CommitParams p;
+  memset(&p, 0, sizeof(p));
+  for (int l = 0; l < n_layers; ++l) {
+    if ((rc = check_layer(&layers[l], sh.hkv))) return rc;
+    p.pools[l] = layers[l].pool;
+    p.pool_pages[l] = layers[l].n_pages;
+  }
+  fill_seq_descs(p.seq, seqs, n_seqs, nullptr);
+  p.n_seqs = n_seqs;
+  p.n_layers = n_layers;
+  p.hkv = sh.hkv;
+  p.T = sh.T;
+  p.page_bytes = layers[0].page_bytes;
+  p.n_commit = n_commit;
+  p.path = path;
+  p.ctx_dev = ctx_dev;
+  p.status = dev_status;
+  return to_status(launch_kv_commit(p, (cudaStream_t)stream));
+}
+
+int stv_int8_qk_dots(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seq, const void* q_row,
+                     int q_head, int32_t tok_begin, int32_t tok_end, int32_t* dots, int32_t* dev_status,
+                     stv_stream_t stream) {
+  ShapeInfo sh;
+  int rc = check_shape(shape, -1, &sh);
+  if (rc) return rc;
+  if ((rc = check_layer(layer, sh.hkv)) || (rc = check_seqs(seq, 1, 0))) return rc;
+  if (!q_row || !dots || q_head < 0 || q_head >= sh.hq) return STV_ERR_INVALID_ARG;
+  if (tok_begin < 0 || tok_end < tok_begin || (int64_t)tok_end > (int64_t)seq->n_pages * kPageTok)
+    return STV_ERR_INVALID_ARG;
+  VerifyParams p;
+  memset(&p, 0, sizeof(p));
+  fill_seq_descs(p.seq, seq, 1, nullptr);
+  p.n_seqs = 1;
+  p.hq = sh.hq;
+  p.hkv = sh.hkv;
+  p.G = sh.G;
+  p.pool = layer->pool;
+  p.page_bytes = layer->page_bytes;
+  p.pool_pages = layer->n_pages;
+  p.status = dev_status;
+  return to_status(launch_int8_dots(p, 0, static_cast<const __half*>(q_row), q_head, tok_begin, tok_end, dots,
+                                    (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,205 @@
+// kv_pack.cu -- a1 kv_append_pack and a7 kv_commit.
+//
+// kv_append_pack quantizes fp16 K/V rows into the paged 3-bit cache ("elpis"
+// README, header table: 3-bit KV cache, 12 KiB per token over 16 layers).
+// One CTA per (row, KV head); thread = channel, warp = one 32-channel group,
+// so the group maximum is one warp reduction and a K block's three words are
+// three warp-wide OR reductions.  V codes are channel-major (a block holds one
+// channel's codes for 32 tokens), so each thread read-modify-writes the three
+// bits of its own channel with atomics (rows appended in the same launch may
+// share a V block; their bits are disjoint).
+//
+// kv_commit moves the accepted rows to ctx .. ctx + n_commit - 1 ("elpis"
+// README, "Why fast": commit the longest matching path + 1).  One CTA per
+// (sequence, layer, KV head) reads every source row into shared memory before
+// writing any destination, because a destination slot can be the source slot
+// of a later row.
+#include "stv_device.cuh"
+
+namespace stv {
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+// 3-bit code of x for scale s (the quantizer of include/stv.h).  x / s is an
+// IEEE single division: a quotient of two fp16 values lands on a half-integer
+// only when it is one, so rounding it half-to-even matches the exact rule.
+__device__ __forceinline__ int quant_code(float x, float s) {
+  if (s == 0.f) return 4;
+  float r = rintf(__fdiv_rn(x, s)) + 4.f;
+  r = fminf(fmaxf(r, 0.f), 7.f);
+  return (int)r;
+}
+
+__global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ AppendParams p) {
+  const int row = blockIdx.x / p.hkv, h = blockIdx.x % p.hkv;
+  const int c = threadIdx.x, g = c >> 5, lane = c & 31;
+  const int s = __ldg(p.row_seq + row), pos = __ldg(p.row_pos + row);
+  if (s < 0 || s >= p.n_seqs || pos < 0) {
+    if (c == 0) report(p.status, STV_DEV_BAD_ROW);
+    return;
+  }
+  uint8_t* hb = const_cast<uint8_t*>(
+      head_block(p.seq[s], p.pool, p.page_bytes, p.pool_pages, pos, h, c == 0 ? p.status : nullptr));
+  if (!hb) return;
+  const int slot = pos & (kPageTok - 1);
+  const int64_t src = ((int64_t)row * p.hkv + h) * kHeadDim + c;
+
+  // ---- K: token-major blocks ----
+  {
+    float x = __half2float(p.k[src]);
+    __half sh = __float2half_rn(warp_max(fabsf(x)) * 0.25f);
+    int code = quant_code(x, __half2float(sh));
+    uint32_t mine[3] = {0u, 0u, 0u};
+#pragma unroll
+    for (int b = 0; b < 3; ++b) {
+      int wd, bt;
+      bit_place(lane, b, wd, bt);
+      if ((code >> b) & 1) mine[wd] |= 1u << bt;
+    }
+    uint32_t w0 = __reduce_or_sync(0xffffffffu, mine[0]);
+    uint32_t w1 = __reduce_or_sync(0xffffffffu, mine[1]);
+    uint32_t w2 = __reduce_or_sync(0xffffffffu, mine[2]);
+    if (lane == 0) {
+      uint32_t* wp = reinterpret_cast<uint32_t*>(hb + kOffKCodes + slot * 96 + g * 12);
+      wp[0] = w0;
+      wp[1] = w1;
+      wp[2] = w2;
+      *reinterpret_cast<__half*>(hb + kOffKScales + slot * 16 + g * 2) = sh;
+    }
+  }
+  // ---- V: channel-major blocks of 32 tokens ----
+  {
+    float x = __half2float(p.v[src]);
+    __half sh = __float2half_rn(warp_max(fabsf(x)) * 0.25f);
+    int code = quant_code(x, __half2float(sh));
+    const int tile = slot / kTileTok, within = slot % kTileTok;
+    uint32_t* wp = reinterpret_cast<uint32_t*>(hb + kOffVCodes + tile * kVTileCodeBytes + c * 24 + (within / 32) * 12);
+    const int i = within % 32;
+#pragma unroll
+    for (int b = 0; b < 3; ++b) {
+      int wd, bt;
+      bit_place(i, b, wd, bt);
+      if ((code >> b) & 1)
+        atomicOr(wp + wd, 1u << bt);
+      else
+        atomicAnd(wp + wd, ~(1u << bt));
+    }
+    if (lane == 0)
+      *reinterpret_cast<__half*>(hb + kOffVScales + tile * kVTileScaleBytes + g * (kTileTok * 2) + within * 2) = sh;
+  }
+}
+
+cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t s) {
+  if (p.n_rows == 0) return cudaSuccess;
+  kv_append_kernel<<<p.n_rows * p.hkv, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) kv_commit_kernel(const __grid_constant__ CommitParams p) {
+  int b = blockIdx.x;
+  const int h = b % p.hkv;
+  b /= p.hkv;
+  const int layer = b % p.n_layers;
+  const int s = b / p.n_layers;
+  const int tid = threadIdx.x;
+  const bool leader = (layer == 0 && h == 0 && tid == 0);
+
+  __shared__ int path_s[kMaxT];
+  __shared__ int n_s, ok_s;
+  __shared__ __align__(16) uint8_t krow[kMaxT][112];  // 96 B codes + 16 B scales
+  __shared__ __align__(4) __half vscale[kMaxT][kGroups];
+  __shared__ uint8_t vcode[kMaxT][kHeadDim];
+
+  if (tid == 0) {
+    int n = __ldg(p.n_commit + s);
+    int ok = (n >= 1 && n <= p.T);
+    int prev = -1;
+    for (int i = 0; ok && i < n; ++i) {
+      int x = __ldg(p.path + (int64_t)s * p.T + i);
+      path_s[i] = x;
+      if ((i == 0 && x != 0) || x <= prev || x >= p.T) ok = 0;
+      prev = x;
+    }
+    n_s = n;
+    ok_s = ok;
+  }
+  __syncthreads();
+  if (!ok_s) {
+    if (leader) report(p.status, STV_DEV_BAD_COMMIT);
+    return;
+  }
+  const int n = n_s;
+  const SeqDesc& sd = p.seq[s];
+  const uint8_t* pool = p.pools[layer];
+  const int32_t pool_pages = p.pool_pages[layer];
+
+  // Read every source row.
+  for (int i = 0; i < n; ++i) {
+    const int64_t src = (int64_t)sd.ctx + path_s[i];
+    const uint8_t* hb = head_block(sd, pool, p.page_bytes, pool_pages, src, h, tid == 0 ? p.status : nullptr);
+    if (!hb) {
+      // leave the rows alone: the sequence's table does not reach them
+      if (tid == 0) ok_s = 0;
+      continue;
+    }
+    const int slot = (int)(src & (kPageTok - 1));
+    if (tid < 6)
+      reinterpret_cast<uint4*>(krow[i])[tid] = reinterpret_cast<const uint4*>(hb + kOffKCodes + slot * 96)[tid];
+    else if (tid == 6)
+      reinterpret_cast<uint4*>(krow[i])[6] = *reinterpret_cast<const uint4*>(hb + kOffKScales + slot * 16);
+    else if (tid >= 8 && tid < 16) {
+      const int g = tid - 8, tile = slot / kTileTok, within = slot % kTileTok;
+      vscale[i][g] =
+          *reinterpret_cast<const __half*>(hb + kOffVScales + tile * kVTileScaleBytes + g * (kTileTok * 2) + within * 2);
+    }
+    {
+      const int tile = slot / kTileTok, within = slot % kTileTok;
+      const uint32_t* wp =
+          reinterpret_cast<const uint32_t*>(hb + kOffVCodes + tile * kVTileCodeBytes + tid * 24 + (within / 32) * 12);
+      vcode[i][tid] = (uint8_t)block_code(wp[0], wp[1], wp[2], within % 32);
+    }
+  }
+  __syncthreads();
+  if (!ok_s) return;
+
+  // Write every destination row.
+  for (int i = 0; i < n; ++i) {
+    const int64_t dst = (int64_t)sd.ctx + i;
+    uint8_t* hb = const_cast<uint8_t*>(head_block(sd, pool, p.page_bytes, pool_pages, dst, h, nullptr));
+    if (!hb) continue;
+    const int slot = (int)(dst & (kPageTok - 1));
+    const int tile = slot / kTileTok, within = slot % kTileTok;
+    if (tid < 6)
+      reinterpret_cast<uint4*>(hb + kOffKCodes + slot * 96)[tid] = reinterpret_cast<const uint4*>(krow[i])[tid];
+    else if (tid == 6)
+      *reinterpret_cast<uint4*>(hb + kOffKScales + slot * 16) = reinterpret_cast<const uint4*>(krow[i])[6];
+    else if (tid >= 8 && tid < 16) {
+      const int g = tid - 8;
+      *reinterpret_cast<__half*>(hb + kOffVScales + tile * kVTileScaleBytes + g * (kTileTok * 2) + within * 2) =
+          vscale[i][g];
+    }
+    // Channel `tid` owns its V words in this head: plain read-modify-write.
+    uint32_t* wp = reinterpret_cast<uint32_t*>(hb + kOffVCodes + tile * kVTileCodeBytes + tid * 24 + (within / 32) * 12);
+    const int code = vcode[i][tid], pos = within % 32;
+#pragma unroll
+    for (int bb = 0; bb < 3; ++bb) {
+      int wd, bt;
+      bit_place(pos, bb, wd, bt);
+      wp[wd] = (wp[wd] & ~(1u << bt)) | ((uint32_t)((code >> bb) & 1) << bt);
+    }
+  }
+  if (leader && p.ctx_dev) p.ctx_dev[s] += n;
+}
+
+cudaError_t launch_kv_commit(const CommitParams& p, cudaStream_t s) {
+  kv_commit_kernel<<<p.n_seqs * p.n_layers * p.hkv, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace stv

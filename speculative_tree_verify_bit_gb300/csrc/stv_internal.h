@@ -1,0 +1,133 @@
+// stv_internal.h -- shared definitions of the CUDA library (host and device):
+// cache layout constants, the split plan, kernel parameter blocks and the
+// launchers that api.cu calls.  Not part of the public ABI (include/stv.h).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/stv.h"
+
+namespace stv {
+
+constexpr int kHeadDim = 256;
+constexpr int kGroup = 32;
+constexpr int kGroups = kHeadDim / kGroup;  // 8
+constexpr int kPageTok = 256;
+constexpr int kTileTok = 64;                 // V-code tiles and verify tiles
+constexpr int kMaxRows = 128;                // T * G per KV head
+constexpr int kMaxT = 32;
+
+// Byte offsets inside one KV head's block of a page (see include/stv.h).
+constexpr int kOffKCodes = 0;
+constexpr int kOffKScales = kPageTok * kGroups * 12;            // 24576
+constexpr int kOffVCodes = kOffKScales + kPageTok * kGroups * 2;  // 28672
+constexpr int kOffVScales = kOffVCodes + kPageTok * kGroups * 12;  // 53248
+constexpr int kHeadBytes = kOffVScales + kPageTok * kGroups * 2;   // 57344
+constexpr int kVTileCodeBytes = kHeadDim * 24;                     // 6144: one 64-token tile
+constexpr int kVTileScaleBytes = kGroups * kTileTok * 2;           // 1024
+constexpr int kKTileCodeBytes = kTileTok * 96;                     // 6144
+constexpr int kKTileScaleBytes = kTileTok * 16;                    // 1024
+static_assert(kHeadBytes == STV_HEAD_BLOCK_BYTES, "layout");
+
+struct SeqDesc {
+  const int32_t* page_table;
+  int32_t n_pages;
+  int32_t ctx;
+  int32_t splits;     // splits per KV head for this sequence
+  int32_t unit_base;  // first work unit of this sequence
+};
+
+// Split plan: every (sequence, KV head) range [0, ctx + T) is cut into pieces
+// of `tiles_per_split` 64-token tiles; each piece is one work unit (one CTA),
+// numbered sequence-major, then KV head, then split.
+struct Plan {
+  int n_units;
+  int tiles_per_split;
+  int splits[STV_MAX_SEQS];
+  int unit_base[STV_MAX_SEQS + 1];
+};
+
+// Workspace carve-up (byte offsets, each 256-aligned).
+struct WsLayout {
+  size_t off_qi, off_sq, off_opart, off_ml, total;
+};
+
+struct ShapeInfo {
+  int hq, hkv, G, T, R;  // R = T * G rows per KV head
+};
+
+// Parameters of one verify launch (passed by value; < 4 KB).
+struct VerifyParams {
+  SeqDesc seq[STV_MAX_SEQS];
+  int n_seqs;
+  int T, hq, hkv, G, R;
+  int tiles_per_split;
+  int n_units;
+  int path;
+  const uint8_t* pool;
+  int64_t page_bytes;
+  int32_t pool_pages;
+  const __half* q;        // [n_seqs][T][hq][256]
+  const int32_t* parent;  // [n_seqs][T]
+  const int8_t* qi;       // [n_seqs][T][hq][256] (int8 path)
+  const float* sq;        // [n_seqs][T][hq]
+  float* o_part;          // [n_units][R][256]
+  float* ml;              // [n_units][R][2] (m in log2 units, l)
+  int32_t* status;
+};
+
+struct CombineParams {
+  SeqDesc seq[STV_MAX_SEQS];
+  int n_seqs;
+  int T, hq, hkv, G, R;
+  const float* o_part;
+  const float* ml;
+  __half* o;
+};
+
+struct AppendParams {
+  SeqDesc seq[STV_MAX_SEQS];
+  int n_seqs;
+  int hkv;
+  uint8_t* pool;
+  int64_t page_bytes;
+  int32_t pool_pages;
+  const __half* k;
+  const __half* v;
+  const int32_t* row_seq;
+  const int32_t* row_pos;
+  int n_rows;
+  int32_t* status;
+};
+
+constexpr int kMaxLayers = 128;
+struct CommitParams {
+  SeqDesc seq[STV_MAX_SEQS];
+  uint8_t* pools[kMaxLayers];
+  int n_seqs, n_layers, hkv, T;
+  int64_t page_bytes;
+  int32_t pool_pages[kMaxLayers];
+  const int32_t* n_commit;
+  const int32_t* path;
+  int32_t* ctx_dev;
+  int32_t* status;
+};
+
+// ---- host helpers (api.cu) ----
+int make_plan(const ShapeInfo& sh, const stv_seq* seqs, int n_seqs, int sm_count, Plan* plan);
+WsLayout ws_layout(const ShapeInfo& sh, int n_seqs, const Plan& plan);
+
+// ---- launchers (return cudaError_t of the launch) ----
+cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t s);
+cudaError_t launch_kv_commit(const CommitParams& p, cudaStream_t s);
+cudaError_t launch_quantize_q(const __half* q, int n_rows, int8_t* qi, float* sq, cudaStream_t s);
+cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);
+cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t s);
+cudaError_t launch_tree_accept(const int32_t* parent, const int32_t* draft, const int32_t* argmax, int T, int n_seqs,
+                               int32_t* n_commit, int32_t* path, int32_t* out_ids, int32_t* status, cudaStream_t s);
+cudaError_t launch_int8_dots(const VerifyParams& p, int seq, const __half* q_row, int q_head, int tok_begin,
+                             int tok_end, int32_t* dots, cudaStream_t s);
+
+}  // namespace stv

@@ -1,0 +1,100 @@
+"""The C-ABI library loads and exports every symbol include/stv.h declares;
+host-side validation and workspace sizing work without a GPU (no compute
+calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_tree_verify_bit_gb300 as stv
+from speculative_tree_verify_bit_gb300 import build as stv_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    stv_build.build()
+    return stv.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "stv.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(stv_\w+)\(", text, re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 10
+    assert set(names) == set(stv.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert stv.status_string(0) == "STV_OK"
+    assert stv.status_string(-3) == "STV_ERR_WORKSPACE_TOO_SMALL"
+    assert stv.status_string(-99) == "STV_ERR_UNKNOWN"
+
+
+def test_page_bytes_and_shape_validation(lib):
+    assert stv.stv_page_bytes(stv.make_shape(24, 4)) == 229376
+    for bad in (stv.stv_shape(24, 4, 128, 32, 256), stv.stv_shape(24, 5, 256, 32, 256),
+                stv.stv_shape(24, 4, 256, 16, 256), stv.stv_shape(24, 4, 256, 32, 128)):
+        with pytest.raises(stv.StvError) as e:
+            stv.stv_page_bytes(bad)
+        assert e.value.status == stv.STV_ERR_SHAPE_UNSUPPORTED
+
+
+def _seqs(ctxs, pages):
+    arr = (stv.stv_seq * len(ctxs))()
+    for i, (c, p) in enumerate(zip(ctxs, pages)):
+        arr[i] = stv.stv_seq(0x1000, p, c)  # a dummy device address: never dereferenced here
+    return arr
+
+
+def _ws(shape, ctxs, pages, t, sm):
+    out = ctypes.c_size_t()
+    rc = stv.load().stv_verify_workspace_bytes(ctypes.byref(shape), _seqs(ctxs, pages), len(ctxs), t, sm,
+                                               ctypes.byref(out))
+    return rc, out.value
+
+
+def test_workspace_bytes_long_context_plan(lib):
+    # 262,144 + 16 keys = 4,097 tiles of 64 per KV head; 4 heads on 152 SMs
+    # -> 108 tiles per split, 38 splits per head, 152 work units.
+    rc, nbytes = _ws(stv.make_shape(), [262144], [1025], 16, 152)
+    assert rc == 0
+    qi = 16 * 24 * 256
+    sq = 16 * 24 * 4
+    opart = 152 * 96 * 256 * 4
+    ml = 152 * 96 * 2 * 4
+    a = lambda x: (x + 255) // 256 * 256
+    assert nbytes == a(a(a(qi) + sq) + opart) + ml
+
+
+def test_workspace_units_never_exceed_sm_count(lib):
+    for ctxs in ([1024], [1 << 20], [1024 << i for i in range(8)], [0] * 64, [7] * 3):
+        pages = [-(-(c + 16) // 256) for c in ctxs]
+        rc1, small = _ws(stv.make_shape(), ctxs, pages, 16, 152)
+        rc2, big = _ws(stv.make_shape(), ctxs, pages, 16, 10_000)
+        assert rc1 == 0 and rc2 == 0 and big >= small
+
+
+@pytest.mark.parametrize("ctxs,pages,t,rc", [
+    ([100], [1], 16, stv.STV_OK),
+    ([250], [1], 16, stv.STV_ERR_INVALID_ARG),    # ctx + T past the pages
+    ([-1], [1], 16, stv.STV_ERR_INVALID_ARG),
+    ([100], [1], 0, stv.STV_ERR_SHAPE_UNSUPPORTED),
+    ([100], [1], 33, stv.STV_ERR_SHAPE_UNSUPPORTED),
+    ([100] * 65, [1] * 65, 16, stv.STV_ERR_INVALID_ARG),
+])
+def test_host_validation(lib, ctxs, pages, t, rc):
+    assert _ws(stv.make_shape(), ctxs, pages, t, 152)[0] == rc
+
+
+def test_rows_per_kv_head_limit(lib):
+    # T * G must stay <= 128: 32 nodes x 6 heads is rejected, 32 x 4 accepted
+    assert _ws(stv.make_shape(24, 4), [10], [1], 32, 152)[0] == stv.STV_ERR_SHAPE_UNSUPPORTED
+    assert _ws(stv.make_shape(16, 4), [10], [1], 32, 152)[0] == stv.STV_OK

@@ -1,0 +1,144 @@
+"""a2..a5 verify_attn + split_combine on the GPU against the fp64 oracle.
+
+Sources: "elpis" README, "Why fast" (8-row token tree verified in one pass;
+decode verify with 3-bit K codes as exact int8); Reddit posts (u/iamMess),
+second post (split-KV verify attention).  Tolerance per (node, Q head) row:
+relative L2 <= 1e-3 and max abs <= 4e-3; int8 dots bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_tree_verify_bit_gb300 as stv
+import workloads
+from roundkit import Round, assert_attention_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("path", ["exact", "int8"])
+def test_tiny_workload_all_rows(gpu, path):
+    """1 layer, context 1,024, 16-node tree of depth <= 8, 24/4 heads: every
+    output row against the oracle."""
+    w = workloads.WORKLOADS["tiny"]
+    r = Round(list(w.ctx), w.t_nodes, seed=workloads.layer_seed(w, 0))
+    r.gpu_cache()
+    r.oracle_cache()
+    got = r.gpu_verify(path).float().cpu().numpy()
+    want = r.oracle_attention(path)
+    assert_attention_close(got, want, f"tiny/{path}")
+
+
+@pytest.mark.parametrize("path", ["exact", "int8"])
+def test_chain_workload_all_rows_and_sequential_decode(gpu, path):
+    """Context 8,192, an 8-node chain: all rows against the oracle, and each
+    node against a one-row decode on the GPU at context ctx + i (the chain
+    verify must equal eight sequential decode steps)."""
+    w = workloads.WORKLOADS["chain"]
+    r = Round(list(w.ctx), w.t_nodes, seed=workloads.layer_seed(w, 0), tree="chain")
+    layer = r.gpu_cache()
+    r.oracle_cache()
+    got = r.gpu_verify(path).float().cpu().numpy()
+    assert_attention_close(got, r.oracle_attention(path), f"chain/{path}")
+    ctx = w.ctx[0]
+    for i in range(w.t_nodes):
+        seqs = [stv.Seq(r.seqs[0].page_table, ctx + i)]
+        ws = torch.empty(stv.stv_verify_workspace_bytes(r.shape, seqs, 1), dtype=torch.uint8, device=gpu)
+        o = torch.empty((1, 1, r.hq, 256), dtype=torch.float16, device=gpu)
+        q = r.q[:, i:i + 1].contiguous()
+        stv.stv_verify_attn(r.shape, layer, seqs, q, torch.tensor([[-1]], dtype=torch.int32, device=gpu), 1, path, ws)
+        stv.stv_split_combine(r.shape, seqs, 1, ws, o)
+        step = o.float().cpu().numpy()[0, 0]
+        assert_attention_close(got[0, i], step, f"chain step {i}")
+
+
+@pytest.mark.parametrize("path", ["exact", "int8"])
+@pytest.mark.parametrize("ctx,t,hq,hkv", [
+    ([0], 16, 24, 4),                 # tree rows only
+    ([1], 1, 24, 4),                  # one-row decode
+    ([300, 0, 1000], 7, 24, 4),       # ragged batch, ragged tails
+    ([511], 32, 16, 4),               # T = 32, 128 rows per KV head
+    ([2000], 16, 8, 1),               # one KV head, G = 8
+])
+def test_edge_shapes(gpu, path, ctx, t, hq, hkv):
+    r = Round(ctx, t, seed=4242 + t + sum(ctx), hq=hq, hkv=hkv)
+    r.gpu_cache()
+    r.oracle_cache()
+    got = r.gpu_verify(path).float().cpu().numpy()
+    assert_attention_close(got, r.oracle_attention(path), f"{ctx}/{t}/{path}")
+
+
+def test_ragged_batch_small(gpu):
+    """The ragged workload's structure (8 requests, contexts doubling from
+    1K, one launch, shared pool with a random page assignment) at contexts
+    1K..8K, one sampled row set per request."""
+    ctx = [1024 << (i % 4) for i in range(8)]
+    r = Round(ctx, 16, seed=1004)
+    r.gpu_cache()
+    r.oracle_cache()
+    got = r.gpu_verify("exact").float().cpu().numpy()
+    rows = [(s, n, h) for s in range(8) for n in (0, 7, 15) for h in (0, 13, 23)]
+    want = r.oracle_attention("exact", rows=rows)
+    g = np.stack([got[s, n, h] for s, n, h in rows])
+    assert_attention_close(g, want, "ragged-small")
+
+
+@pytest.mark.parametrize("name", ["tree32k", "long262k", "ragged"])
+def test_full_size_sampled_rows(gpu, name):
+    """Full-size workloads, one layer, in the benchmark's launch configuration:
+    sampled rows against the oracle."""
+    w = workloads.WORKLOADS[name]
+    r = Round(list(w.ctx), w.t_nodes, seed=workloads.layer_seed(w, 0))
+    r.gpu_cache()
+    r.oracle_cache()
+    for path in ("exact", "int8"):
+        got = r.gpu_verify(path).float().cpu().numpy()
+        rows = [(s, n, h) for s in range(r.n_seqs) for n, h in ((0, 0), (15, 23), (9, 11))]
+        if name == "ragged":
+            rows = [(s, n, h) for s in (0, 5, 7) for n, h in ((0, 0), (15, 23))]
+        want = r.oracle_attention(path, rows=rows)
+        g = np.stack([got[s, n, h] for s, n, h in rows])
+        assert_attention_close(g, want, f"{name}/{path}")
+
+
+def test_int8_dots_bit_exact(gpu):
+    r = Round([700], 16, seed=77)
+    layer = r.gpu_cache()
+    r.oracle_cache()
+    qn = r.q.cpu().numpy()
+    for node, qh in ((0, 0), (5, 11), (15, 23)):
+        q_row = r.q[0, node, qh].contiguous()
+        dots = torch.zeros((716, 8), dtype=torch.int32, device=gpu)
+        stv.stv_int8_qk_dots(r.shape, layer, r.seqs[0], q_row, qh, 0, 716, dots)
+        torch.cuda.synchronize()
+        want = oracle.int8_dots(r.ocache, r.tables, 0, qn[0, node, qh], qh, r.hq, 0, 716)
+        assert np.array_equal(dots.cpu().numpy(), want)
+
+
+def test_deterministic_run_to_run(gpu):
+    r = Round([5000, 3000], 16, seed=5)
+    r.gpu_cache()
+    a = r.gpu_verify("exact")
+    b = r.gpu_verify("exact")
+    assert torch.equal(a, b)
+
+
+def test_bad_tree_flagged(gpu):
+    r = Round([100], 4, seed=6, parents=[[-1, 0, 5, 1]])
+    r.gpu_cache()
+    ws = torch.empty(stv.stv_verify_workspace_bytes(r.shape, r.seqs, 4), dtype=torch.uint8, device=gpu)
+    status = torch.zeros(1, dtype=torch.int32, device=gpu)
+    stv.stv_verify_attn(r.shape, r.layer, r.seqs, r.q, torch.as_tensor(r.parent, device=gpu), 4, "exact", ws,
+                        dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & stv.STV_DEV_BAD_TREE
+
+
+def test_workspace_too_small_rejected(gpu):
+    r = Round([100], 4, seed=7)
+    r.gpu_cache()
+    need = stv.stv_verify_workspace_bytes(r.shape, r.seqs, 4)
+    ws = torch.empty(need - 256, dtype=torch.uint8, device=gpu)
+    with pytest.raises(stv.StvError) as e:
+        stv.stv_verify_attn(r.shape, r.layer, r.seqs, r.q, torch.as_tensor(r.parent, device=gpu), 4, "exact", ws)
+    assert e.value.status == stv.STV_ERR_WORKSPACE_TOO_SMALL
