@@ -1,0 +1,431 @@
+"""Benchmark of one speculative tree-verify round over a paged 3-bit KV cache.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long262k]
+                    [--path exact|int8] [--impl ours|reference]
+
+A step is one whole verify round of the workload: for each of the 16
+attention layers, append the tree's T rows to the 3-bit cache
+(stv_kv_append_pack), run the tree-masked split-KV verify attention
+(stv_verify_attn) and merge its splits (stv_split_combine); then greedy tree
+acceptance (stv_tree_accept) and compaction of the accepted rows in every
+layer (stv_kv_commit).  The metric is microseconds per layer-round (the
+round's time / 16), with the packed KV bytes the round streams per
+layer-round and their rate (GB/s) against the HBM roofline.
+
+Inputs are seeded synthetic tensors (workloads.py), resident in HBM before
+the timed region.  The cache of 16 layers x 224 MiB (262K context) is far
+larger than L2 (129 MB), so no flush is needed between steps.
+
+Multi-GPU: the round does not need an exchange between GPUs, so N GPUs run N
+independent replicas (one process per GPU under torchrun); value aggregates
+their layer-rounds over the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle (the only other implementation of
+this method that exists here) on the host cores, on a bounded sample of the
+same workload, scaled to the same unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "verify-attn us/layer-round and HBM GB/s (% of roofline) at 32K and 262K ctx"
+UNIT = "us/layer-round"
+
+
+def algorithmic_bytes_per_layer_round(ctx_list, t, hq=24, hkv=4):
+    """Packed KV streamed by verify (768 B codes + 128 B scales per token over
+    4 KV heads) plus Q in and O out."""
+    kv = sum(c + t for c in ctx_list) * hkv * (2 * 96 + 2 * 16)
+    qo = len(ctx_list) * 2 * t * hq * 256 * 2
+    return kv + qo
+
+
+def verify_kernel_bytes(ctx_list, t, hq=24, hkv=4):
+    """Bytes one verify launch must read: packed KV of every visible key and Q."""
+    return sum(c + t for c in ctx_list) * hkv * (2 * 96 + 2 * 16) + len(ctx_list) * t * hq * 256 * 2
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for k in ("hbm_gbs", "hbm_GBs", "hbm"):
+                if k in d and d[k]:
+                    v = d[k]
+                    v = v.get("value", v.get("burst")) if isinstance(v, dict) else v
+                    return float(v), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.samples = []
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                self.samples.append(f)
+
+    def summary(self):
+        if not getattr(self, "samples", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(f[1]) for f in self.samples if f[1].replace(".", "").isdigit()]
+        mx = [float(f[2]) for f in self.samples if f[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for f in self.samples:
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(self.samples)}
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+class GpuRound:
+    """All layers of one workload resident on the GPU, plus one round's inputs."""
+
+    def __init__(self, w: workloads.Workload, p_accept: float, device, layers: int | None = None):
+        import torch
+
+        import speculative_tree_verify_bit_gb300 as stv
+
+        self.stv, self.torch, self.w, self.dev = stv, torch, w, device
+        self.L = layers or w.layers
+        self.T, self.hq, self.hkv = w.t_nodes, w.hq, w.hkv
+        self.shape = stv.make_shape(self.hq, self.hkv)
+        self.pool_pages, tables = workloads.page_tables_for(w)
+        self.tables = tables
+        self.seqs = [stv.Seq(torch.as_tensor(t, device=device), c) for t, c in zip(tables, w.ctx)]
+        self.ctx = list(w.ctx)
+        rt = workloads.round_trees(w, p_accept)
+        self.parent = torch.as_tensor(rt.parent, device=device)
+        self.draft = torch.as_tensor(rt.draft, device=device)
+        self.argmax = torch.as_tensor(rt.argmax, device=device)
+        T, n = self.T, w.n_seqs
+        self.layers, self.q, self.k_tree, self.v_tree = [], [], [], []
+        row_seq_ctx = torch.cat([torch.full((c,), s, dtype=torch.int32, device=device) for s, c in enumerate(w.ctx)])
+        row_pos_ctx = torch.cat([torch.arange(c, dtype=torch.int32, device=device) for c in w.ctx])
+        self.row_seq = torch.cat([torch.full((T,), s, dtype=torch.int32, device=device) for s in range(n)])
+        self.row_pos = torch.cat([torch.arange(c, c + T, dtype=torch.int32, device=device) for c in w.ctx])
+        for l in range(self.L):
+            seed = workloads.layer_seed(w, l)
+            layer = stv.LayerCache.empty(self.pool_pages, self.hkv, device=device)
+            ks, vs, kt, vt = [], [], [], []
+            for s, c in enumerate(w.ctx):
+                k, v = workloads.kv_rows(seed + 7919 * s, c + T, self.hkv, device=device)
+                ks.append(k[:c]); vs.append(v[:c]); kt.append(k[c:]); vt.append(v[c:])
+            kc, vc = torch.cat(ks).contiguous(), torch.cat(vs).contiguous()
+            stv.stv_kv_append_pack(self.shape, layer, self.seqs, kc, vc, row_seq_ctx, row_pos_ctx)
+            del kc, vc, ks, vs
+            self.layers.append(layer)
+            self.k_tree.append(torch.cat(kt).contiguous())
+            self.v_tree.append(torch.cat(vt).contiguous())
+            self.q.append(workloads.q_rows(seed, n, T, self.hq, device=device).contiguous())
+        torch.cuda.synchronize()
+        self.ws_bytes = stv.stv_verify_workspace_bytes(self.shape, self.seqs, T)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.o = torch.empty((n, T, self.hq, 256), dtype=torch.float16, device=device)
+        self.n_commit = torch.zeros(n, dtype=torch.int32, device=device)
+        self.path = torch.zeros((n, T), dtype=torch.int32, device=device)
+        self.out_ids = torch.zeros((n, T), dtype=torch.int32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def launches_per_step(self, path):
+        return self.L * (3 + (1 if path == "int8" else 0)) + 2
+
+    def step(self, path, verify_events=None):
+        stv = self.stv
+        for l in range(self.L):
+            stv.stv_kv_append_pack(self.shape, self.layers[l], self.seqs, self.k_tree[l], self.v_tree[l],
+                                   self.row_seq, self.row_pos, dev_status=self.status)
+            if verify_events is not None:
+                verify_events[l][0].record()
+            stv.stv_verify_attn(self.shape, self.layers[l], self.seqs, self.q[l], self.parent, self.T, path, self.ws,
+                                dev_status=self.status)
+            if verify_events is not None:
+                verify_events[l][1].record()
+            stv.stv_split_combine(self.shape, self.seqs, self.T, self.ws, self.o)
+        stv.stv_tree_accept(self.parent, self.draft, self.argmax, self.n_commit, self.path, self.out_ids,
+                            dev_status=self.status)
+        stv.stv_kv_commit(self.shape, self.layers, self.seqs, self.T, self.n_commit, self.path,
+                          dev_status=self.status)
+
+
+def e2e_step(r: GpuRound, host, path):
+    """The same round through the public API with host buffers: copy the
+    round's inputs in from pinned memory, run it, read the accepted tokens."""
+    torch = r.torch
+    for l in range(r.L):
+        r.q[l].copy_(host["q"][l], non_blocking=True)
+        r.k_tree[l].copy_(host["k"][l], non_blocking=True)
+        r.v_tree[l].copy_(host["v"][l], non_blocking=True)
+    r.parent.copy_(host["parent"], non_blocking=True)
+    r.draft.copy_(host["draft"], non_blocking=True)
+    r.argmax.copy_(host["argmax"], non_blocking=True)
+    r.step(path)
+    host["n_commit"].copy_(r.n_commit, non_blocking=True)
+    host["out_ids"].copy_(r.out_ids, non_blocking=True)
+
+
+def run_gpu(args, rank, world):
+    import torch
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = workloads.WORKLOADS[args.workload]
+    p_accept = args.p_accept if args.p_accept is not None else w.p_accept[-1 if args.workload == "long262k" else 0]
+    r = GpuRound(w, p_accept, dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        r.step(args.path)
+    ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(r.L)]
+    per_step_verify = []
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(dev.index) as clk:
+        start.record()
+        for _ in range(args.steps):
+            r.step(args.path, verify_events=ev)
+            per_step_verify.append(ev)
+            ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(r.L)]
+        end.record()
+        barrier()
+    total_ms = start.elapsed_time(end)
+    verify_ms = [a.elapsed_time(b) for e in per_step_verify for a, b in e]
+    st = int(r.status.item())
+
+    # e2e: host buffers, copies inside the timed region
+    host = {
+        "q": [x.cpu().pin_memory() for x in r.q], "k": [x.cpu().pin_memory() for x in r.k_tree],
+        "v": [x.cpu().pin_memory() for x in r.v_tree], "parent": r.parent.cpu().pin_memory(),
+        "draft": r.draft.cpu().pin_memory(), "argmax": r.argmax.cpu().pin_memory(),
+        "n_commit": torch.zeros_like(r.n_commit, device="cpu").pin_memory(),
+        "out_ids": torch.zeros_like(r.out_ids, device="cpu").pin_memory(),
+    }
+    h2d = sum(x.numel() * x.element_size() for k in ("q", "k", "v") for x in host[k]) + sum(
+        host[k].numel() * 4 for k in ("parent", "draft", "argmax"))
+    d2h = host["n_commit"].numel() * 4 + host["out_ids"].numel() * 4
+    for _ in range(2):
+        e2e_step(r, host, args.path)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step(r, host, args.path)
+    e1.record()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+
+    times = torch.tensor([total_ms, e2e_ms], device=dev)
+    if dist is not None:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms = float(times[0]), float(times[1])
+    layer_rounds = args.steps * r.L * world
+    us_per_lr = total_ms * 1e3 / layer_rounds
+    e2e_us = e2e_ms * 1e3 / layer_rounds
+    bytes_lr = algorithmic_bytes_per_layer_round(w.ctx, w.t_nodes, w.hq, w.hkv)
+    vbytes = verify_kernel_bytes(w.ctx, w.t_nodes, w.hq, w.hkv)
+    v_us = statistics.mean(verify_ms) * 1e3
+    peak, peak_kind = measured_peak()
+    achieved = vbytes / (v_us * 1e-6) / 1e9
+    traffic = load_traffic(args.workload, args.path)
+    return dict(rank=rank, us_per_lr=us_per_lr, e2e_us=e2e_us, bytes_lr=bytes_lr, v_us=v_us, vbytes=vbytes,
+                peak=peak, peak_kind=peak_kind, achieved=achieved, clocks=clk.summary(), status=st, h2d=h2d,
+                d2h=d2h, launches=r.launches_per_step(args.path) * args.steps, p_accept=p_accept, traffic=traffic,
+                n_units=None, ws_bytes=r.ws_bytes, round_gbs=bytes_lr / (us_per_lr * 1e-6) / 1e9 / world)
+
+
+def load_traffic(workload, path):
+    """dram bytes per verify launch from the committed ncu summary, if any."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return d.get(f"{workload}/{path}")
+        except Exception:
+            return None
+    return None
+
+
+# --------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle on the host cores, bounded sample
+# --------------------------------------------------------------------------
+
+def oracle_sample(w: workloads.Workload, n_rows: int, threads: int):
+    """Time the oracle on n_rows (node, Q head) rows of layer 0 over the full
+    context; scale to microseconds per layer-round (all T * hq rows of every
+    sequence).  The oracle's own cache is packed first (set-up, untimed)."""
+    import torch
+
+    import oracle
+
+    T, hq, hkv = w.t_nodes, w.hq, w.hkv
+    pool_pages, tables = workloads.page_tables_for(w)
+    cache = oracle.Cache(hkv, pool_pages)
+    seed = workloads.layer_seed(w, 0)
+    # the sample covers the largest sequence (the long-context share dominates)
+    s = int(np.argmax(w.ctx))
+    c = w.ctx[s]
+    k, v = workloads.kv_rows(seed + 7919 * s, c + T, hkv, device="cpu" if not torch.cuda.is_available() else "cuda")
+    k, v = k.cpu().numpy(), v.cpu().numpy()
+    oracle.kv_append(cache, [tables[i] if i == s else np.zeros(0, np.int32) for i in range(len(tables))], k, v,
+                     np.full(c + T, s, np.int32), np.arange(c + T, dtype=np.int32))
+    q = workloads.q_rows(seed, w.n_seqs, T, hq, device="cpu").numpy()
+    rt = workloads.round_trees(w)
+    rows = [(s, n % T, (n * 7) % hq) for n in range(n_rows)]
+    ctx = [c if i == s else 0 for i in range(w.n_seqs)]
+    tabs = [tables[i] if i == s else np.zeros(1, np.int32) for i in range(len(tables))]
+    t0 = time.perf_counter()
+    oracle.attention(cache, tabs, ctx, q, rt.parent, hq, "exact", rows=rows, n_threads=threads)
+    dt = time.perf_counter() - t0
+    keys_sampled = n_rows * (c + T)
+    keys_all = sum(cc + T for cc in w.ctx) * T * hq
+    us_per_lr = dt * 1e6 * keys_all / keys_sampled
+    sample = (f"oracle attention (fp64, exact path) for {n_rows} of {T * hq * w.n_seqs} (node, Q head) rows of "
+              f"layer 0 over the {c}-key context of sequence {s}, scaled by visible keys to one full layer-round")
+    return us_per_lr, dt, sample
+
+
+def run_reference(args):
+    w = workloads.WORKLOADS[args.workload]
+    threads = os.cpu_count() or 1
+    vals = []
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm state; warm-up steps are not repeated
+    n_rows = args.oracle_rows
+    for _ in range(max(1, args.steps)):
+        v, dt, sample = oracle_sample(w, n_rows, threads)
+        vals.append(v)
+        if dt > 60:
+            break
+    val = statistics.median(vals)
+    line = {
+        "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus, "steps": len(vals),
+        "warmup": args.warmup, "ms_per_step": val * w.layers / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "ctx": list(w.ctx), "t_nodes": w.t_nodes, "layers": w.layers, "hq": w.hq,
+                   "hkv": w.hkv, "head_dim": 256},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="long262k", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--path", default="exact", choices=["exact", "int8"])
+    ap.add_argument("--p-accept", type=float, default=None)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--oracle-rows", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    res = run_gpu(args, rank, world)
+    if rank != 0:
+        return
+    w = workloads.WORKLOADS[args.workload]
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        threads = os.cpu_count() or 1
+        v, dt, sample = oracle_sample(w, args.oracle_rows, threads)
+        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+    frac = res["achieved"] / res["peak"]
+    line = {
+        "metric": METRIC, "value": res["us_per_lr"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["us_per_lr"] * w.layers * world / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": w.name, "ctx": list(w.ctx), "t_nodes": w.t_nodes, "layers": w.layers, "hq": w.hq,
+                   "hkv": w.hkv, "head_dim": 256, "path": args.path, "p_accept": res["p_accept"],
+                   "l2": "inputs larger than L2 (16 layers of packed KV)", "parallelism": f"replicas{world}"},
+        "gbs_per_layer_round": res["round_gbs"],
+        "bytes_per_layer_round": res["bytes_lr"],
+        "verify_us_per_launch": res["v_us"],
+        "roofline": {"bound": "hbm", "achieved": res["achieved"], "peak": res["peak"], "unit": "GB/s",
+                     "frac": frac, "traffic": res["traffic"], "kernel": "verify_attn",
+                     "algorithmic_bytes_per_launch": res["vbytes"], "peak_source": res["peak_kind"]},
+        "cpu_baseline": cpu,
+        "e2e": {"value": res["e2e_us"], "unit": UNIT, "h2d_bytes_per_step": res["h2d"],
+                "d2h_bytes_per_step": res["d2h"]},
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+        "dev_status": res["status"],
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

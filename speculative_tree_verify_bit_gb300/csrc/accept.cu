@@ -39,7 +39,9 @@ __global__ void __launch_bounds__(32) tree_accept_kernel(const int32_t* __restri
     return;
   }
   const int pl = par < 0 ? 0 : par;  // lane holding the parent
-  const bool match = (i == 0) || (act && dr == __shfl_sync(full, am, pl));
+  // Every lane executes the shuffle (no short-circuit around a collective).
+  const int parent_am = __shfl_sync(full, am, pl);
+  const bool match = (i == 0) || (act && dr == parent_am);
 
   // ok: every edge root -> i matches; depth: edges from the root.
   int ok = (i == 0) ? 1 : 0, depth = 0;
