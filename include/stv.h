@@ -213,6 +213,28 @@ int stv_int8_qk_dots(const stv_shape* shape, const stv_layer_cache* layer, const
                      int q_head, int32_t tok_begin, int32_t tok_end, int32_t* dots, int32_t* dev_status,
                      stv_stream_t stream);
 
+/*
+ * Verify attention and split merge in one call, without a caller workspace
+ * (no counterpart on the pages: it exists for callers of this library that
+ * cannot allocate device memory -- e.g. a serving engine whose allocator
+ * already owns nearly all device memory, where an extra cudaMalloc during a
+ * decode step can fail, or a plain C host without a device allocator).
+ * Same arguments, checks and results as stv_verify_attn followed by
+ * stv_split_combine, with o as in stv_split_combine.  The scratch is a
+ * fixed 32 MiB array inside the library: it calls no cudaMalloc, cudaFree
+ * or allocating routine, and every GPU that loads the library keeps those
+ * 32 MiB until the process exits.  A round whose workspace
+ * (stv_verify_workspace_bytes) exceeds 32 MiB returns
+ * STV_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.  All calls share the
+ * array: calls that overlap on the GPU (other streams or host threads) race
+ * and must be serialised by the caller.  The first call on each device looks
+ * the array's device address up (a CUDA runtime query, once per device) and
+ * should come before any stream capture.
+ */
+int stv_verify_attn_no_alloc(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs, int n_seqs,
+                             const void* q, const int32_t* parent, int t_nodes, int path, void* o,
+                             int32_t* dev_status, stv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -41,6 +41,7 @@ HEAD_BLOCK_BYTES = 57344
 EXPORTS = (
     "stv_status_string", "stv_version", "stv_page_bytes", "stv_kv_append_pack", "stv_verify_workspace_bytes",
     "stv_verify_attn", "stv_split_combine", "stv_tree_accept", "stv_kv_commit", "stv_int8_qk_dots",
+    "stv_verify_attn_no_alloc",
 )
 
 
@@ -94,6 +95,8 @@ def load() -> ctypes.CDLL:
         lib.stv_kv_commit.argtypes = [P, P, I, P, I, I, P, P, P, P, P]
         lib.stv_int8_qk_dots.restype = I
         lib.stv_int8_qk_dots.argtypes = [P, P, P, P, I, I32, I32, P, P, P]
+        lib.stv_verify_attn_no_alloc.restype = I
+        lib.stv_verify_attn_no_alloc.argtypes = [P, P, P, I, P, P, I, I, P, P, P]
         _lib = lib
     return _lib
 
@@ -268,3 +271,18 @@ def stv_int8_qk_dots(shape, layer: LayerCache, seq: Seq, q_row, q_head: int, tok
         ctypes.byref(shape), ctypes.byref(lc), ctypes.byref(sc), _ptr(q_row, torch.float16, "q_row"), int(q_head),
         int(tok_begin), int(tok_end), _ptr(dots, torch.int32, "dots"), _ptr(dev_status, torch.int32, "dev_status"),
         _stream(stream)))
+
+
+def stv_verify_attn_no_alloc(shape, layer: LayerCache, seqs, q, parent, t_nodes: int, path, o, dev_status=None,
+                             stream=None):
+    """Verify attention + split merge with the library's own fixed scratch
+    (for callers that cannot allocate device memory; see include/stv.h)."""
+    import torch
+
+    lc = layer.c()
+    arr = _seq_array(seqs)
+    path = PATHS.get(path, path)
+    _check("stv_verify_attn_no_alloc", load().stv_verify_attn_no_alloc(
+        ctypes.byref(shape), ctypes.byref(lc), arr, len(seqs), _ptr(q, torch.float16, "q"),
+        _ptr(parent, torch.int32, "parent"), int(t_nodes), int(path), _ptr(o, torch.float16, "o"),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
