@@ -221,7 +221,7 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(dev)
     w = workloads.WORKLOADS[args.workload]
     p_accept = args.p_accept if args.p_accept is not None else w.p_accept[-1 if args.workload == "long262k" else 0]
-    r = GpuRound(w, p_accept, dev)
+    r = GpuRound(w, p_accept, dev, layers=args.layers)
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -378,6 +378,7 @@ def main():
     ap.add_argument("--p-accept", type=float, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--oracle-rows", type=int, default=32)
+    ap.add_argument("--layers", type=int, default=None, help="fewer layers (profiling captures only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -406,10 +407,10 @@ def main():
     frac = res["achieved"] / res["peak"]
     line = {
         "metric": METRIC, "value": res["us_per_lr"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": res["us_per_lr"] * w.layers * world / 1e3, "higher_is_better": False,
+        "warmup": args.warmup, "ms_per_step": res["us_per_lr"] * (args.layers or w.layers) * world / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": w.name, "ctx": list(w.ctx), "t_nodes": w.t_nodes, "layers": w.layers, "hq": w.hq,
-                   "hkv": w.hkv, "head_dim": 256, "path": args.path, "p_accept": res["p_accept"],
+        "config": {"workload": w.name, "ctx": list(w.ctx), "t_nodes": w.t_nodes, "layers": args.layers or w.layers,
+                   "hq": w.hq, "hkv": w.hkv, "head_dim": 256, "path": args.path, "p_accept": res["p_accept"],
                    "l2": "inputs larger than L2 (16 layers of packed KV)", "parallelism": f"replicas{world}"},
         "gbs_per_layer_round": res["round_gbs"],
         "bytes_per_layer_round": res["bytes_lr"],

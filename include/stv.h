@@ -85,6 +85,7 @@ enum stv_dev_status {
   STV_DEV_BAD_TREE = 2,   /* parent[0] != -1 or parent[i] outside [0, i) */
   STV_DEV_BAD_ROW = 4,    /* row_seq outside [0, n_seqs) or row_pos negative */
   STV_DEV_BAD_COMMIT = 8, /* n_commit outside [1, T] or path not a root path */
+  STV_DEV_TIMEOUT = 16,   /* a bounded wait inside a kernel gave up; outputs are invalid */
 };
 
 enum stv_path { STV_PATH_EXACT = 0, STV_PATH_INT8 = 1 };

@@ -26,6 +26,7 @@ STV_DEV_BAD_PAGE = 1
 STV_DEV_BAD_TREE = 2
 STV_DEV_BAD_ROW = 4
 STV_DEV_BAD_COMMIT = 8
+STV_DEV_TIMEOUT = 16
 
 STV_PATH_EXACT = 0
 STV_PATH_INT8 = 1

@@ -7,7 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/stv.h"
+#include "stv.h"
 
 namespace stv {
 

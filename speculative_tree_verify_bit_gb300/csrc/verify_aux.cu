@@ -1,0 +1,141 @@
+// verify_aux.cu -- the kernels around the tensor-core verify kernel: the int8
+// Q quantizer (a3), split_combine (a5) and the int8-dots inspection kernel.
+//
+// Sources: "elpis" README, "Why fast" (8-row token tree verified in one pass;
+// decode verify with 3-bit K codes as exact int8 against int8 Q); Reddit
+// posts (u/iamMess), second post (split-KV verify attention).
+//
+// The int8-dots kernel decodes K with the same block decoder as the verify
+// kernel and accumulates the per-group products of qi and (code - 4) as
+// integers, so its output can be compared bit for bit.
+#include "stv_device.cuh"
+
+namespace stv {
+
+__device__ __forceinline__ float wmax(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+// a3: per (node, Q head) row, m = max|q|, qi = rne(127 q / m), sQ = m / 127.
+// 127 q is exact in fp32 and the quotient of two fp16-derived values never
+// rounds onto a half-integer, so this matches the exact definition.
+__device__ __forceinline__ void quantize_q_row_warp(const __half* __restrict__ q, int8_t* qi, float* sq) {
+  const int lane = threadIdx.x & 31;
+  uint4 raw = *reinterpret_cast<const uint4*>(q + lane * 8);
+  const __half* hv = reinterpret_cast<const __half*>(&raw);
+  float x[8], m = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    x[e] = __half2float(hv[e]);
+    m = fmaxf(m, fabsf(x[e]));
+  }
+  m = wmax(m);
+  uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    int v = (m == 0.f) ? 0 : (int)rintf(__fdiv_rn(127.f * x[e], m));
+    packed[e >> 2] |= ((uint32_t)(v & 0xff)) << (8 * (e & 3));
+  }
+  *reinterpret_cast<uint2*>(qi + lane * 8) = make_uint2(packed[0], packed[1]);
+  if (lane == 0) *sq = (m == 0.f) ? 0.f : __fdiv_rn(m, 127.f);
+}
+
+__global__ void __launch_bounds__(256) quantize_q_kernel(const __half* __restrict__ q, int n_rows,
+                                                         int8_t* __restrict__ qi, float* __restrict__ sq) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= n_rows) return;
+  quantize_q_row_warp(q + (int64_t)row * kHeadDim, qi + (int64_t)row * kHeadDim, sq + row);
+}
+
+cudaError_t launch_quantize_q(const __half* q, int n_rows, int8_t* qi, float* sq, cudaStream_t s) {
+  quantize_q_kernel<<<(n_rows + 7) / 8, 256, 0, s>>>(q, n_rows, qi, sq);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// a5: split_combine.  One warp per (sequence, KV head, row); lane = 8 channels.
+
+__global__ void __launch_bounds__(256) split_combine_kernel(const __grid_constant__ CombineParams p) {
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  int s = 0, base = 0;
+  while (s < p.n_seqs && gw >= base + p.hkv * p.R) {
+    base += p.hkv * p.R;
+    ++s;
+  }
+  if (s >= p.n_seqs) return;
+  const int h = (gw - base) / p.R, r = (gw - base) % p.R;
+  const SeqDesc& sd = p.seq[s];
+  const int u0 = sd.unit_base + h * sd.splits;
+  float M = -INFINITY;
+  for (int k = 0; k < sd.splits; ++k) M = fmaxf(M, p.ml[((int64_t)(u0 + k) * p.R + r) * 2]);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, L = 0.f;
+  for (int k = 0; k < sd.splits; ++k) {
+    const int64_t at = (int64_t)(u0 + k) * p.R + r;
+    const float mk = p.ml[at * 2];
+    if (mk == -INFINITY) continue;
+    const float wk = exp2f(mk - M);
+    L += wk * p.ml[at * 2 + 1];
+    const float4* src = reinterpret_cast<const float4*>(p.o_part + at * kHeadDim + lane * 8);
+    const float4 a = src[0], b = src[1];
+    acc[0] += wk * a.x; acc[1] += wk * a.y; acc[2] += wk * a.z; acc[3] += wk * a.w;
+    acc[4] += wk * b.x; acc[5] += wk * b.y; acc[6] += wk * b.z; acc[7] += wk * b.w;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  __align__(16) __half outv[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) outv[e] = __float2half_rn(acc[e] * inv);
+  const int node = r / p.G, qh = h * p.G + r % p.G;
+  *reinterpret_cast<uint4*>(p.o + (((int64_t)s * p.T + node) * p.hq + qh) * kHeadDim + lane * 8) =
+      *reinterpret_cast<const uint4*>(outv);
+}
+
+cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t s) {
+  int rows = 0;
+  for (int i = 0; i < p.n_seqs; ++i) rows += p.hkv * p.R;
+  split_combine_kernel<<<(rows + 7) / 8, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Inspection: exact int8 per-group dots of one Q row against a key range.
+
+__global__ void __launch_bounds__(256) int8_dots_kernel(const __grid_constant__ VerifyParams p, int s,
+                                                        const __half* __restrict__ q_row, int q_head, int tok_begin,
+                                                        int tok_end, int32_t* __restrict__ dots) {
+  __shared__ __align__(16) int8_t qi[kHeadDim];
+  __shared__ float sq;
+  if (threadIdx.x < 32) quantize_q_row_warp(q_row, qi, &sq);
+  __syncthreads();
+  const int h = q_head / p.G;
+  const int n = tok_end - tok_begin;
+  for (int idx = blockIdx.x * 256 + threadIdx.x; idx < n * kGroups; idx += gridDim.x * 256) {
+    const int j = idx / kGroups, g = idx % kGroups, tok = tok_begin + j;
+    const uint8_t* hb = head_block(p.seq[s], p.pool, p.page_bytes, p.pool_pages, tok, h, p.status);
+    int acc = 0;
+    if (hb) {
+      const int slot = tok & (kPageTok - 1);
+      const uint32_t* wp = reinterpret_cast<const uint32_t*>(hb + kOffKCodes + slot * 96 + g * 12);
+      __half2 out[16];
+      decode_block_raw(wp[0], wp[1], wp[2], out);
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        float2 f = __half22float2(out[m]);
+        acc += (int)qi[g * kGroup + 2 * m] * (int)f.x + (int)qi[g * kGroup + 2 * m + 1] * (int)f.y;
+      }
+    }
+    dots[idx] = acc;
+  }
+}
+
+cudaError_t launch_int8_dots(const VerifyParams& p, int seq, const __half* q_row, int q_head, int tok_begin,
+                             int tok_end, int32_t* dots, cudaStream_t s) {
+  const int n = (tok_end - tok_begin) * kGroups;
+  if (n <= 0) return cudaSuccess;
+  int blocks = (n + 255) / 256;
+  if (blocks > 1024) blocks = 1024;
+  int8_dots_kernel<<<blocks, 256, 0, s>>>(p, seq, q_row, q_head, tok_begin, tok_end, dots);
+  return cudaGetLastError();
+}
+
+}  // namespace stv

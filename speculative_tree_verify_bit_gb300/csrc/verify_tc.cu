@@ -1,0 +1,597 @@
+// verify_tc.cu -- a2..a4 on the 5th-generation tensor cores (tcgen05, TMEM,
+// bulk async copies): split-KV, tree-masked GQA verify attention over the
+// paged 3-bit cache.
+//
+// Sources: "elpis" README, "Why fast" (8-row token tree verified in one pass;
+// decode verify with the 3-bit K codes as exact int8 against int8 Q; prefill
+// K/V double-buffered ring: the next tile loads while the current one is
+// computed); Reddit posts (u/iamMess), second post (split-KV verify kernel).
+// The pages' kernels target the RTX 3090 (mma.sync, IMMA); this one is laid
+// out for sm_103a.
+//
+// One CTA per work unit (sequence, KV head, range of 64-key tiles), one CTA
+// per SM, 14 warps:
+//   warp 0      producer: one bulk copy per array per tile (K codes, K scales,
+//               V codes, V scales: 14,336 B) into a 4-stage shared ring.
+//   warp 1      TMEM owner and MMA issuer (the warp runs the loop, one
+//               elected lane issues).
+//   warps 2-5   softmax: thread = query row = TMEM lane (128 rows, the
+//               T*G rows sharing the KV head, zero-padded).
+//   warps 6-13  unpack: 3-bit codes -> fp16 operands in shared memory.
+// Tensor memory (512 columns): Q [0,128) as the A operand of S = Q K^T;
+// S0/S1 [128,192) [192,256), double-buffered, where P (fp16) overwrites S as
+// the A operand of O += P V; O [256,512) fp32 accumulators.
+// Shared memory: K (64 keys x 256 ch) and V^T (256 ch x 64 keys) fp16
+// operands, 128-byte swizzled K-major, double-buffered; the raw ring.
+// Both paths use the fp16 tensor pipe (sm_103a has no kind::i8): the int8
+// path feeds qi (integers, exact in fp16) and scales the scores by sQ.
+// Softmax is online in fp32 with a stale-maximum threshold: P uses a
+// reference maximum that is raised (rescaling O and l) only when a score
+// exceeds it by more than 2^8, so P <= 256 in fp16 and O rescales are rare.
+// Every wait is bounded; a timeout sets a CTA abort flag, every role stops,
+// in-flight copies and MMAs are waited for (bounded) and TMEM is freed.
+#include "stv_device.cuh"
+
+namespace stv {
+namespace {
+
+constexpr int kThreads = 448;
+constexpr int kStages = 4;
+constexpr int kStageBytes = kKTileCodeBytes + kKTileScaleBytes + kVTileCodeBytes + kVTileScaleBytes;  // 14336
+constexpr int kOperandBytes = 32768;  // one K or V^T fp16 tile
+constexpr int kSmemBytes = 1024 /*align slack*/ + 4 * kOperandBytes + kStages * kStageBytes + 1024 /*barriers etc*/;
+constexpr uint32_t kWaitLimit = 1u << 20;   // try_wait calls before a wait gives up
+constexpr uint32_t kSuspendHintNs = 20000;  // per try_wait
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleThreshold = 8.f;  // log2 units
+
+constexpr uint32_t kColQ = 0, kColS0 = 128, kColO = 256, kTmemCols = 512;
+
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4)                     // D: f32
+         | ((uint32_t)(N >> 3) << 17)  // N
+         | ((uint32_t)(M >> 4) << 24);  // M; A, B f16 K-major
+}
+constexpr uint32_t kIdescQK = idesc_f16_f32(128, 64);
+constexpr uint32_t kIdescPV = idesc_f16_f32(128, 256);
+
+struct Bars {
+  uint64_t raw_full[kStages], raw_empty[kStages];
+  uint64_t kd_full[2], kd_empty[2], vd_full[2], vd_empty[2];
+  uint64_t s_full[2], p_full[2];
+  uint64_t pv_done, q_ready, mma_done;
+  uint32_t tmem_base;
+  int abort;
+  uint32_t anc[kMaxT];
+};
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+// try_wait suspends the thread (up to the hint, in ns) until the phase
+// completes, so a waiting warp does not take issue slots from working ones.
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait by one thread.  False on timeout or when the CTA aborted.
+__device__ __forceinline__ bool wait1(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+  for (uint32_t it = 0; it < kWaitLimit; ++it) {
+    if (mbar_try(b, parity)) return true;
+    if ((it & 63) == 63 && *abort_flag) return false;
+  }
+  *abort_flag = 1;
+  return false;
+}
+// Bounded wait by a whole warp; the result is warp-uniform.
+__device__ __forceinline__ bool waitw(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+  bool ok = wait1(b, parity, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   su32(dst)),
+               "l"(src), "r"(bytes), "r"(su32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, __half2 a, __half2 b, __half2 c, __half2 d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(h2u(a)), "r"(h2u(b)), "r"(h2u(c)), "r"(h2u(d))
+               : "memory");
+}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Issued by one elected lane of a converged warp: the warp runs the MMA loop
+// in uniform control flow, so descriptors stay in uniform registers.
+__device__ __forceinline__ void tc_commit(uint64_t* b) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(su32(b))
+      : "memory");
+}
+__device__ __forceinline__ void mma_tmemA(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.u32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+      "r"(a), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+#define STV_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+#define STV_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
+
+// 32 consecutive 32-bit columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%"
+      "19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : STV_R8(0), STV_R8(8), STV_R8(16), STV_R8(24)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      STV_W8(0), STV_W8(8), STV_W8(16), STV_W8(24)
+      : "memory");
+}
+// Wait for this thread's TMEM loads; the registers are ordered after the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: 128-byte swizzle, K-major, 8-row groups
+// 1024 bytes apart (stride byte offset), sm_100-family version field.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// 128-byte-swizzled K-major tile: rows of 128 bytes in 8-row groups of 1024
+// bytes; 16-byte chunk c of row `row` sits at chunk c ^ (row % 8).  A row's
+// base with its XOR term folded in makes each chunk address one XOR.
+__device__ __forceinline__ uint32_t sw128_row(int row) {
+  return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((row & 7) << 4));
+}
+__device__ __forceinline__ uint32_t sw128_chunk(uint32_t row_base, int c) { return row_base ^ (uint32_t)(c << 4); }
+
+// 2^x with the SFU's approximate exponential (inputs here are <= 8; results
+// below the normal range flush to zero, which a softmax weight can afford).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_constant__ VerifyParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment of the operand tiles (the swizzle works on address bits).
+  const uint32_t base_u32 = su32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024 - (base_u32 & 1023)) & 1023);
+  uint8_t* const kdeq0 = smem;                      // K tiles: kdeq0 + b * kOperandBytes
+  uint8_t* const vdeq0 = smem + 2 * kOperandBytes;  // V^T tiles: vdeq0 + b * kOperandBytes
+  uint8_t* ring = smem + 4 * kOperandBytes;
+  Bars* bars = reinterpret_cast<Bars*>(ring + kStages * kStageBytes);
+  volatile int* abort_flag = &bars->abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- locate the work unit ----
+  int s = 0;
+  while (s + 1 < p.n_seqs && (int)blockIdx.x >= p.seq[s + 1].unit_base) ++s;
+  const SeqDesc sd = p.seq[s];
+  const int local = blockIdx.x - sd.unit_base;
+  const int h = local / sd.splits, split = local % sd.splits;
+  const int T = p.T, G = p.G, R = p.R;
+  const int tok0 = split * p.tiles_per_split * kTileTok;
+  const int tok1 = min(sd.ctx + T, tok0 + p.tiles_per_split * kTileTok);
+  const int n_tiles = (tok1 - tok0 + kTileTok - 1) / kTileTok;
+
+  // ---- set-up ----
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bars->raw_full[i], 1);
+      mbar_init(&bars->raw_empty[i], 8);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->kd_full[i], 8);
+      mbar_init(&bars->kd_empty[i], 1);
+      mbar_init(&bars->vd_full[i], 8);
+      mbar_init(&bars->vd_empty[i], 1);
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->p_full[i], 4);
+    }
+    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->q_ready, 4);
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (tid < T) {  // a2: ancestor-or-self masks
+    uint32_t m = 1u << tid;
+    int n = tid;
+    const int32_t* par = p.parent + (int64_t)s * T;
+    for (int st = 0; st < T && n > 0; ++st) {
+      int pa = __ldg(par + n);
+      if (pa < 0 || pa >= n) {
+        if (split == 0 && h == 0) report(p.status, STV_DEV_BAD_TREE);
+        break;
+      }
+      m |= 1u << pa;
+      n = pa;
+    }
+    if (tid == 0 && __ldg(par) != -1 && split == 0 && h == 0) report(p.status, STV_DEV_BAD_TREE);
+    bars->anc[tid] = m;
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&bars->tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_before();
+  __syncthreads();
+  tc_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // =================== producer ===================
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int st = i % kStages;
+        if (!wait1(&bars->raw_empty[st], ((i / kStages) & 1) ^ 1, abort_flag)) break;
+        const int key0 = tok0 + i * kTileTok;
+        const int64_t lp = key0 >> 8;
+        int32_t page = lp < sd.n_pages ? __ldg(sd.page_table + lp) : -1;
+        if (page < 0 || page >= p.pool_pages) {
+          report(p.status, STV_DEV_BAD_PAGE);
+          page = 0;  // read a valid page; the result is flagged as garbage
+        }
+        const uint8_t* hb = p.pool + (int64_t)page * p.page_bytes + (int64_t)h * kHeadBytes;
+        const int t = (key0 & (kPageTok - 1)) / kTileTok;
+        uint8_t* dst = ring + st * kStageBytes;
+        uint64_t* bar = &bars->raw_full[st];
+        mbar_expect_tx(bar, kStageBytes);
+        bulk_g2s(dst, hb + kOffKCodes + t * kKTileCodeBytes, kKTileCodeBytes, bar);
+        bulk_g2s(dst + kKTileCodeBytes, hb + kOffKScales + t * kKTileScaleBytes, kKTileScaleBytes, bar);
+        bulk_g2s(dst + kKTileCodeBytes + kKTileScaleBytes, hb + kOffVCodes + t * kVTileCodeBytes, kVTileCodeBytes,
+                 bar);
+        bulk_g2s(dst + kKTileCodeBytes + kKTileScaleBytes + kVTileCodeBytes, hb + kOffVScales + t * kVTileScaleBytes,
+                 kVTileScaleBytes, bar);
+        issued = i + 1;
+      }
+      // No copy may still be landing when the CTA exits.
+      for (int i = max(0, issued - kStages); i < issued; ++i) {
+        volatile int never = 0;
+        wait1(&bars->raw_full[i % kStages], (i / kStages) & 1, &never);
+      }
+    }
+  } else if (warp == 1) {
+    // =================== MMA issuer (whole warp, one elected lane issues) ===================
+    const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
+    bool ok = waitw(&bars->q_ready, 0, abort_flag);
+    tc_after();
+    // Issue order: QK(0), QK(1), then PV(j), QK(j+2) for j = 0, 1, ...
+    // S is double-buffered: QK(j+2) overwrites the columns that held P(j),
+    // after PV(j) in the tensor pipe's order, while softmax(j+1) runs.
+    // Descriptors are built once; each MMA then only adds a constant to the
+    // start-address field (no carry: shared addresses are < 256 KiB).
+    // Rebuilding them per MMA made the issue loop, which competes with the
+    // unpack and softmax warps for issue slots, slower than the tensor pipe.
+    const uint64_t kdesc0 = desc_sw128(su32(kdeq0)), vdesc0 = desc_sw128(su32(vdeq0));
+    auto issue_qk = [&](int i) -> bool {
+      const int b = i & 1;
+      if (!waitw(&bars->kd_full[b], (i >> 1) & 1, abort_flag)) return false;
+      tc_after();
+      const uint64_t kd = kdesc0 + (uint64_t)(b * (kOperandBytes >> 4));
+      const uint32_t d = tm + kColS0 + 64 * b;
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk)
+        mma_tmemA(d, tm + kColQ + 8 * kk, kd + (uint64_t)((kk >> 2) * 512 + (kk & 3) * 2), kIdescQK, kk > 0);
+      tc_commit(&bars->kd_empty[b]);
+      tc_commit(&bars->s_full[b]);
+      return true;
+    };
+    for (int i = 0; ok && i < 2 && i < n_tiles; ++i) ok = issue_qk(i);
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      const int b = j & 1;
+      if (!(ok = waitw(&bars->p_full[b], (j >> 1) & 1, abort_flag))) break;
+      if (!(ok = waitw(&bars->vd_full[b], (j >> 1) & 1, abort_flag))) break;
+      tc_after();
+      const uint64_t vd = vdesc0 + (uint64_t)(b * (kOperandBytes >> 4));
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_tmemA(tm + kColO, tm + kColS0 + 64 * b + 8 * kk, vd + (uint64_t)(kk * 2), kIdescPV, (j > 0 || kk > 0));
+      tc_commit(&bars->vd_empty[b]);
+      tc_commit(&bars->pv_done);
+      if (j + 2 < n_tiles) ok = issue_qk(j + 2);
+    }
+    // Every MMA issued here has finished before TMEM is freed.
+    tc_commit(&bars->mma_done);
+    volatile int never = 0;
+    waitw(&bars->mma_done, 0, &never);
+  } else if (warp < 6) {
+    // =================== softmax (thread = row = TMEM lane) ===================
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
+    const bool int8 = p.path == STV_PATH_INT8;
+    float c = kLog2e / 16.f;
+    int node = 0;
+    // Q row -> TMEM columns [0, 128)
+    {
+      int64_t qrow = 0;
+      const bool live = r < R;
+      if (live) {
+        node = r / G;
+        qrow = ((int64_t)s * T + node) * p.hq + h * G + r % G;
+        if (int8) c *= p.sq[qrow];
+      }
+#pragma unroll
+      for (int chunk = 0; chunk < 4; ++chunk) {
+        uint32_t v[32];
+        if (!live) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        } else if (!int8) {
+          const uint4* src = reinterpret_cast<const uint4*>(p.q + qrow * kHeadDim + chunk * 64);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            uint4 x = __ldg(src + e);
+            v[4 * e] = x.x;
+            v[4 * e + 1] = x.y;
+            v[4 * e + 2] = x.z;
+            v[4 * e + 3] = x.w;
+          }
+        } else {
+          const int8_t* src = p.qi + qrow * kHeadDim + chunk * 64;
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            v[e] = h2u(__halves2half2(__int2half_rn(src[2 * e]), __int2half_rn(src[2 * e + 1])));
+        }
+        tmem_st32(lane_addr + kColQ + 32 * chunk, v);
+      }
+      tmem_wait_st();
+      tc_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->q_ready);
+    }
+    const uint32_t anc = bars->anc[node];
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int b = i & 1;
+      if (!(ok = waitw(&bars->s_full[b], (i >> 1) & 1, abort_flag))) break;
+      tc_after();
+      uint32_t sa[32], sb[32];
+      tmem_ld32(lane_addr + kColS0 + 64 * b, sa);
+      tmem_ld32(lane_addr + kColS0 + 64 * b + 32, sb);
+      tmem_wait_ld(sa);
+      tmem_wait_ld(sb);
+      const int key0 = tok0 + i * kTileTok;
+      if (key0 + kTileTok > sd.ctx || key0 + kTileTok > tok1) {
+        // Visibility of the tile's 64 keys as one bit mask: context keys,
+        // this row's ancestor-or-self tree keys, nothing at or past tok1.
+        // Masked keys become -inf by selection (their S may be garbage).
+        const int rel_ctx = sd.ctx - key0, rel_end = tok1 - key0;
+        const uint64_t ctxm = rel_ctx >= 64 ? ~0ull : (rel_ctx <= 0 ? 0ull : ((1ull << rel_ctx) - 1));
+        const uint64_t treem = rel_ctx >= 64 ? 0ull
+                               : (rel_ctx >= 0 ? ((uint64_t)anc << rel_ctx) : ((uint64_t)anc >> (-rel_ctx)));
+        const uint64_t livem = rel_end >= 64 ? ~0ull : ((1ull << rel_end) - 1);
+        const uint64_t vis = (ctxm | treem) & livem;
+        const uint32_t va = (uint32_t)vis, vb = (uint32_t)(vis >> 32);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          sa[e] = ((va >> e) & 1u) ? sa[e] : 0xff800000u;
+          sb[e] = ((vb >> e) & 1u) ? sb[e] : 0xff800000u;
+        }
+      }
+      // Row maximum: 3-input max, 8 independent chains.
+      float mx8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(__uint_as_float(sa[k]), __uint_as_float(sb[k]));
+#pragma unroll
+      for (int e = 8; e < 32; e += 2) {
+        mx8[(e >> 1) & 7] = max3(mx8[(e >> 1) & 7], __uint_as_float(sa[e]), __uint_as_float(sa[e + 1]));
+        mx8[((e >> 1) + 4) & 7] = max3(mx8[((e >> 1) + 4) & 7], __uint_as_float(sb[e]), __uint_as_float(sb[e + 1]));
+      }
+      const float mx = fmaxf(max3(mx8[0], mx8[1], mx8[2]), max3(max3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+      const float m_tile = mx * c;
+      float corr = 1.f;
+      if (m_tile > m_ref + kRescaleThreshold) {
+        if (m_ref != -INFINITY) corr = ex2(m_ref - m_tile);
+        m_ref = m_tile;
+        l *= corr;
+      }
+      // P = 2^(S c - m_ref) in fp16, packed key pairs, into the S columns.
+      const float mref = m_ref == -INFINITY ? 0.f : m_ref;
+      float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float p0 = ex2(fmaf(__uint_as_float(sa[2 * e]), c, -mref));
+        const float p1 = ex2(fmaf(__uint_as_float(sa[2 * e + 1]), c, -mref));
+        const float p2 = ex2(fmaf(__uint_as_float(sb[2 * e]), c, -mref));
+        const float p3 = ex2(fmaf(__uint_as_float(sb[2 * e + 1]), c, -mref));
+        sum8[e & 7] += (p0 + p1) + (p2 + p3);
+        sa[e] = h2u(__floats2half2_rn(p0, p1));
+        sb[e] = h2u(__floats2half2_rn(p2, p3));
+      }
+      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+      uint32_t pk[32];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        pk[e] = sa[e];
+        pk[16 + e] = sb[e];
+      }
+      tmem_st32(lane_addr + kColS0 + 64 * b, pk);
+      // O may be rescaled only once P.V of the previous tile has finished.
+      if (i >= 1) {
+        if (!(ok = waitw(&bars->pv_done, (i - 1) & 1, abort_flag))) break;
+        tc_after();
+        if (__any_sync(0xffffffffu, corr != 1.f)) {
+#pragma unroll 1
+          for (int chunk = 0; chunk < 8; ++chunk) {
+            uint32_t o[32];
+            tmem_ld32(lane_addr + kColO + 32 * chunk, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+            tmem_st32(lane_addr + kColO + 32 * chunk, o);
+          }
+        }
+      }
+      tmem_wait_st();
+      tc_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full[b]);
+    }
+    // ---- epilogue: O, m, l of this row into the workspace ----
+    if (ok && n_tiles >= 1) ok = waitw(&bars->pv_done, (n_tiles - 1) & 1, abort_flag);
+    if (ok) {
+      tc_after();
+      float* dst = p.o_part + ((int64_t)blockIdx.x * R + r) * kHeadDim;
+#pragma unroll 1
+      for (int chunk = 0; chunk < 8; ++chunk) {
+        uint32_t o[32];
+        tmem_ld32(lane_addr + kColO + 32 * chunk, o);
+        tmem_wait_ld(o);
+        if (r < R) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            reinterpret_cast<float4*>(dst + 32 * chunk)[e] =
+                make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]), __uint_as_float(o[4 * e + 2]),
+                            __uint_as_float(o[4 * e + 3]));
+        }
+      }
+      if (r < R) {
+        p.ml[((int64_t)blockIdx.x * R + r) * 2] = m_ref;
+        p.ml[((int64_t)blockIdx.x * R + r) * 2 + 1] = l;
+      }
+    }
+  } else {
+    // =================== unpack (256 threads) ===================
+    const int ut = tid - 6 * 32;
+    // K: key and 64-channel column block.  Each group of 8 consecutive lanes
+    // takes 8 different keys of one column block, so the 8 lanes of a
+    // 128-bit store phase land on 8 different swizzled 16-byte positions.
+    const int kj = (ut >> 5) * 8 + (ut & 7), kcb = (ut >> 3) & 3;
+    const int vch = ut;  // V: channel
+    for (int i = 0; i < n_tiles; ++i) {
+      const int st = i % kStages, b = i & 1;
+      const uint8_t* stage = ring + st * kStageBytes;
+      if (!waitw(&bars->raw_full[st], (i / kStages) & 1, abort_flag)) break;
+      const int key0 = tok0 + i * kTileTok;
+      // ---- K: key kj, groups 2*kcb and 2*kcb+1 -> one 128-byte swizzled row ----
+      if (!waitw(&bars->kd_empty[b], ((i >> 1) & 1) ^ 1, abort_flag)) break;
+      {
+        const uint2* wv = reinterpret_cast<const uint2*>(stage + kj * 96 + kcb * 24);
+        const uint2 w01 = wv[0], w23 = wv[1], w45 = wv[2];
+        const __half2 sc2 = *reinterpret_cast<const __half2*>(stage + kKTileCodeBytes + kj * 16 + kcb * 4);
+        const uint32_t krow = su32(kdeq0) + b * kOperandBytes + kcb * 8192 + sw128_row(kj);
+        const __half2 s0 = __low2half2(sc2), s1 = __high2half2(sc2);
+        __half2 out[16];
+        decode_block_h2(w01.x, w01.y, w23.x, [&](int) { return s0; }, out);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          st_shared_v4(sw128_chunk(krow, q4), out[4 * q4], out[4 * q4 + 1], out[4 * q4 + 2], out[4 * q4 + 3]);
+        decode_block_h2(w23.y, w45.x, w45.y, [&](int) { return s1; }, out);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          st_shared_v4(sw128_chunk(krow, 4 + q4), out[4 * q4], out[4 * q4 + 1], out[4 * q4 + 2], out[4 * q4 + 3]);
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->kd_full[b]);
+      // ---- V: channel vch, 64 keys -> one 128-byte swizzled row of V^T ----
+      if (!waitw(&bars->vd_empty[b], ((i >> 1) & 1) ^ 1, abort_flag)) break;
+      {
+        const uint2* wv = reinterpret_cast<const uint2*>(stage + kKTileCodeBytes + kKTileScaleBytes + vch * 24);
+        const uint2 w01 = wv[0], w23 = wv[1], w45 = wv[2];
+        // this channel's group: 64 key scales, as 32 (key 2m, 2m+1) pairs
+        const uint4* sp = reinterpret_cast<const uint4*>(stage + kKTileCodeBytes + kKTileScaleBytes +
+                                                         kVTileCodeBytes + (vch >> 5) * (kTileTok * 2));
+        const int live = tok1 - key0;  // keys at or beyond this are zeroed
+        const uint32_t vrow = su32(vdeq0) + b * kOperandBytes + sw128_row(vch);
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          uint32_t sc[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 x = sp[blk * 4 + q];
+            sc[4 * q] = x.x;
+            sc[4 * q + 1] = x.y;
+            sc[4 * q + 2] = x.z;
+            sc[4 * q + 3] = x.w;
+          }
+          __half2 out[16];
+          if (blk == 0)
+            decode_block_h2(w01.x, w01.y, w23.x, [&](int m) { return u32_as_h2(sc[m]); }, out);
+          else
+            decode_block_h2(w23.y, w45.x, w45.y, [&](int m) { return u32_as_h2(sc[m]); }, out);
+          if (live < 64) {
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+              const int k0 = blk * 32 + 2 * m;
+              if (k0 >= live) out[m] = __floats2half2_rn(0.f, 0.f);
+              else if (k0 + 1 >= live) out[m] = __halves2half2(__low2half(out[m]), __float2half_rn(0.f));
+            }
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            st_shared_v4(sw128_chunk(vrow, blk * 4 + q4), out[4 * q4], out[4 * q4 + 1], out[4 * q4 + 2], out[4 * q4 + 3]);
+        }
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars->vd_full[b]);
+        mbar_arrive(&bars->raw_empty[st]);
+      }
+    }
+  }
+
+  // ---- teardown ----
+  tc_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+  if (tid == 0 && bars->abort) report(p.status, STV_DEV_TIMEOUT);
+}
+
+}  // namespace
+
+cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  verify_tc_kernel<<<p.n_units, kThreads, kSmemBytes, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace stv
