@@ -97,10 +97,27 @@ __device__ __forceinline__ bool wait1(uint64_t* b, uint32_t parity, volatile int
   *abort_flag = 1;
   return false;
 }
+// Non-blocking check of a phase.  Even a completed phase costs a waiting
+// warp a shared-memory round trip (a few hundred cycles under load), so a
+// warp that needs several barriers checks them all at once, letting the
+// round trips overlap, and then settles each one: `settle` blocks only if
+// some lane saw that phase incomplete.  A phase seen complete stays so until
+// the warp's own next arrival, so an early check remains valid.
+__device__ __forceinline__ uint32_t probe(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+               : "=r"(ok) : "r"(su32(b)), "r"(parity) : "memory");
+  return ok;
+}
 // Bounded wait by a whole warp; the result is warp-uniform.
 __device__ __forceinline__ bool waitw(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
   bool ok = wait1(b, parity, abort_flag);
   return __all_sync(0xffffffffu, ok);
+}
+// Completes a `probe`: true at once when every lane saw the phase complete.
+__device__ __forceinline__ bool settle(uint64_t* b, uint32_t parity, uint32_t probed, volatile int* abort_flag) {
+  if (__all_sync(0xffffffffu, probed)) return true;
+  return waitw(b, parity, abort_flag);
 }
 
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -306,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
     const uint64_t kdesc0 = desc_sw128(su32(kdeq0)), vdesc0 = desc_sw128(su32(vdeq0));
     auto issue_qk = [&](int i) -> bool {
       const int b = i & 1;
-      if (!waitw(&bars->kd_full[b], (i >> 1) & 1, abort_flag)) return false;
+      if (!settle(&bars->kd_full[b], (i >> 1) & 1, probe(&bars->kd_full[b], (i >> 1) & 1), abort_flag)) return false;
       tc_after();
       const uint64_t kd = kdesc0 + (uint64_t)(b * (kOperandBytes >> 4));
       const uint32_t d = tm + kColS0 + 64 * b;
@@ -320,8 +337,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
     for (int i = 0; ok && i < 2 && i < n_tiles; ++i) ok = issue_qk(i);
     for (int j = 0; ok && j < n_tiles; ++j) {
       const int b = j & 1;
-      if (!(ok = waitw(&bars->p_full[b], (j >> 1) & 1, abort_flag))) break;
-      if (!(ok = waitw(&bars->vd_full[b], (j >> 1) & 1, abort_flag))) break;
+      const uint32_t pr_p = probe(&bars->p_full[b], (j >> 1) & 1);
+      const uint32_t pr_v = probe(&bars->vd_full[b], (j >> 1) & 1);
+      if (!(ok = settle(&bars->p_full[b], (j >> 1) & 1, pr_p, abort_flag))) break;
+      if (!(ok = settle(&bars->vd_full[b], (j >> 1) & 1, pr_v, abort_flag))) break;
       tc_after();
       const uint64_t vd = vdesc0 + (uint64_t)(b * (kOperandBytes >> 4));
 #pragma unroll
@@ -449,11 +468,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
         pk[16 + e] = sb[e];
       }
       tmem_st32(lane_addr + kColS0 + 64 * b, pk);
-      // O may be rescaled only once P.V of the previous tile has finished.
-      if (i >= 1) {
+      // O may be rescaled only once P.V of the previous tile has finished, so
+      // a warp that rescales waits for it; the others go on.  P.V(i-2) is
+      // done (QK(i) followed it) and P.V(i) waits for this warp, so pv_done
+      // is in phase i-1 or i and the parity wait is unambiguous.
+      if (i >= 1 && __any_sync(0xffffffffu, corr != 1.f)) {
         if (!(ok = waitw(&bars->pv_done, (i - 1) & 1, abort_flag))) break;
         tc_after();
-        if (__any_sync(0xffffffffu, corr != 1.f)) {
+        {
 #pragma unroll 1
           for (int chunk = 0; chunk < 8; ++chunk) {
             uint32_t o[32];
@@ -471,7 +493,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
       if (lane == 0) mbar_arrive(&bars->p_full[b]);
     }
     // ---- epilogue: O, m, l of this row into the workspace ----
-    if (ok && n_tiles >= 1) ok = waitw(&bars->pv_done, (n_tiles - 1) & 1, abort_flag);
+    // pv_done may be up to three phases behind here, which a parity wait
+    // cannot tell apart; mma_done completes once, after every MMA.
+    if (ok) ok = waitw(&bars->mma_done, 0, abort_flag);
     if (ok) {
       tc_after();
       float* dst = p.o_part + ((int64_t)blockIdx.x * R + r) * kHeadDim;
@@ -504,10 +528,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
     for (int i = 0; i < n_tiles; ++i) {
       const int st = i % kStages, b = i & 1;
       const uint8_t* stage = ring + st * kStageBytes;
-      if (!waitw(&bars->raw_full[st], (i / kStages) & 1, abort_flag)) break;
+      const uint32_t pr_raw = probe(&bars->raw_full[st], (i / kStages) & 1);
+      const uint32_t pr_kd = probe(&bars->kd_empty[b], ((i >> 1) & 1) ^ 1);
+      const uint32_t pr_vd = probe(&bars->vd_empty[b], ((i >> 1) & 1) ^ 1);
+      if (!settle(&bars->raw_full[st], (i / kStages) & 1, pr_raw, abort_flag)) break;
       const int key0 = tok0 + i * kTileTok;
       // ---- K: key kj, groups 2*kcb and 2*kcb+1 -> one 128-byte swizzled row ----
-      if (!waitw(&bars->kd_empty[b], ((i >> 1) & 1) ^ 1, abort_flag)) break;
+      if (!settle(&bars->kd_empty[b], ((i >> 1) & 1) ^ 1, pr_kd, abort_flag)) break;
       {
         const uint2* wv = reinterpret_cast<const uint2*>(stage + kj * 96 + kcb * 24);
         const uint2 w01 = wv[0], w23 = wv[1], w45 = wv[2];
@@ -528,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->kd_full[b]);
       // ---- V: channel vch, 64 keys -> one 128-byte swizzled row of V^T ----
-      if (!waitw(&bars->vd_empty[b], ((i >> 1) & 1) ^ 1, abort_flag)) break;
+      if (!settle(&bars->vd_empty[b], ((i >> 1) & 1) ^ 1, pr_vd, abort_flag)) break;
       {
         const uint2* wv = reinterpret_cast<const uint2*>(stage + kKTileCodeBytes + kKTileScaleBytes + vch * 24);
         const uint2 w01 = wv[0], w23 = wv[1], w45 = wv[2];
