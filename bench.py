@@ -75,53 +75,102 @@ def measured_peak():
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples during the timed region."""
+    """SM clock, power and clock-event reasons sampled during the timed
+    region, through NVML (read-only queries: nothing is changed on the GPU).
+    A thread polls every 5 ms; the device is found by its PCI bus id, so the
+    samples are the GPU this process runs on whatever CUDA_VISIBLE_DEVICES
+    says.  Without NVML it falls back to `nvidia-smi -lms`."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        self.dev, self.period = device_index, period_s
+        self.samples, self.max_mhz, self.source = [], None, None
+
+    def _nvml_open(self):
+        import ctypes
+
+        import torch
+
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit")
+        pr = torch.cuda.get_device_properties(self.dev)
+        bus = f"{getattr(pr, 'pci_domain_id', 0):08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0".encode()
+        h = ctypes.c_void_p()
+        if nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByPciBusId")
+        self.nv, self.h, self.ct = nv, h, ctypes
+        self.reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # 1 = SM clock
+            self.max_mhz = float(mx.value)
+
+    def _nvml_sample(self):
+        ct, nv, h = self.ct, self.nv, self.h
+        mhz, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        ok = nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz)) == 0
+        nv.nvmlDeviceGetPowerUsage(h, ct.byref(mw))
+        self.reasons_fn(h, ct.byref(rs))
+        if ok:
+            self.samples.append((float(mhz.value), mw.value / 1000.0, int(rs.value)))
 
     def __enter__(self):
+        import threading
+
+        self.stop = threading.Event()
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._nvml_open()
+            self._nvml_sample()  # one sample before the timed region starts
+            self.source = "nvml"
+
+            def run():
+                while not self.stop.wait(self.period):
+                    self._nvml_sample()
+
+            self.thread = threading.Thread(target=run, daemon=True)
+            self.thread.start()
         except Exception:
-            self.proc = None
+            self.thread = None
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.dev), "--query-gpu=clocks.sm,clocks.max.sm,power.draw",
+                     "--format=csv,noheader,nounits", "-lms", "100"], stdout=subprocess.PIPE,
+                    stderr=subprocess.DEVNULL, text=True)
+                self.source = "nvidia-smi"
+            except Exception:
+                self.proc = None
         return self
 
     def __exit__(self, *a):
-        self.samples = []
-        if self.proc is None:
-            return
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except Exception:
-            self.proc.kill()
-            out = ""
-        for line in out.strip().splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) >= 9:
-                self.samples.append(f)
+        self.stop.set()
+        if getattr(self, "thread", None) is not None:
+            self.thread.join()
+            self._nvml_sample()  # and one after it
+            self.nv.nvmlShutdown()
+        elif getattr(self, "proc", None) is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            for line in (out or "").strip().splitlines():
+                f = [x.strip() for x in line.split(",")]
+                try:
+                    self.samples.append((float(f[0]), float(f[2]), 0))
+                    self.max_mhz = float(f[1])
+                except (ValueError, IndexError):
+                    pass
 
     def summary(self):
-        if not getattr(self, "samples", None):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(f[1]) for f in self.samples if f[1].replace(".", "").isdigit()]
-        mx = [float(f[2]) for f in self.samples if f[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = set()
-        for f in self.samples:
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(self.samples)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"], "samples": 0}
+        reasons = sorted({n for _, _, r in self.samples for bit, n in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(m for m, _, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples),
+                "power_w_max": max(w for _, w, _ in self.samples), "source": self.source}
 
 
 # --------------------------------------------------------------------------
@@ -291,15 +340,22 @@ def run_gpu(args, rank, world):
 
 
 def load_traffic(workload, path):
-    """dram bytes per verify launch from the committed ncu summary, if any."""
+    """DRAM bytes per verify launch from the committed ncu summary, or None
+    when there is none for this workload or the verify kernel's source has
+    changed since the counters were taken."""
+    import hashlib
+
     p = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(p):
-        try:
-            d = json.load(open(p))
-            return d.get(f"{workload}/{path}")
-        except Exception:
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        src = os.path.join(ROOT, "speculative_tree_verify_bit_gb300", "csrc", "verify_tc.cu")
+        if d.get("verify_tc_sha256") != hashlib.sha256(open(src, "rb").read()).hexdigest():
             return None
-    return None
+        return d.get(f"{workload}/{path}")
+    except Exception:
+        return None
 
 
 # --------------------------------------------------------------------------
@@ -371,7 +427,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="long262k", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--path", default="exact", choices=["exact", "int8"])
