@@ -138,6 +138,9 @@ int stv_kv_append_pack(const stv_shape* shape, const stv_layer_cache* layer, con
  * outputs (fp32), their row maxima and sums, the int8 Q rows and scales.
  * sm_count: SMs the split plan targets; 0 = the current device's count
  * (stv_verify_attn and stv_split_combine always plan for the current device).
+ * The plan cuts each (sequence, KV head) key range into splits of equal
+ * whole 64-key tiles: as many work units as SMs at most, and never more
+ * than 256 splits for one (sequence, KV head).
  */
 int stv_verify_workspace_bytes(const stv_shape* shape, const stv_seq* seqs, int n_seqs, int t_nodes, int sm_count,
                                size_t* bytes);

@@ -3,6 +3,8 @@
 // entry point allocates, frees or synchronises.
 #include <string.h>
 
+#include <algorithm>
+
 #include "stv_internal.h"
 
 namespace stv {
@@ -60,6 +62,8 @@ int make_plan(const ShapeInfo& sh, const stv_seq* seqs, int n_seqs, int sm_count
   const int64_t target = sm_count > 0 ? sm_count : 1;
   int64_t k = (total + target - 1) / target;
   if (k < 1) k = 1;
+  for (int s = 0; s < n_seqs; ++s)  // at most kMaxSplitsPerHead splits per (sequence, KV head)
+    k = std::max<int64_t>(k, (tiles[s] + kMaxSplitsPerHead - 1) / kMaxSplitsPerHead);
   for (;;) {
     int64_t units = 0;
     for (int s = 0; s < n_seqs; ++s) units += sh.hkv * ((tiles[s] + k - 1) / k);
@@ -171,7 +175,7 @@ int stv_verify_workspace_bytes(const stv_shape* shape, const stv_seq* seqs, int 
   if (!bytes || sm_count < 0) return STV_ERR_INVALID_ARG;
   if (sm_count == 0 && (rc = device_sm_count(&sm_count))) return rc;
   Plan plan;
-  make_plan(sh, seqs, n_seqs, sm_count, &plan);
+  if ((rc = make_plan(sh, seqs, n_seqs, sm_count, &plan))) return rc;
   *bytes = ws_layout(sh, n_seqs, plan).total;
   return STV_OK;
 }
@@ -187,7 +191,7 @@ int stv_verify_attn(const stv_shape* shape, const stv_layer_cache* layer, const 
   int sm = 0;
   if ((rc = device_sm_count(&sm))) return rc;
   Plan plan;
-  make_plan(sh, seqs, n_seqs, sm, &plan);
+  if ((rc = make_plan(sh, seqs, n_seqs, sm, &plan))) return rc;
   const WsLayout wl = ws_layout(sh, n_seqs, plan);
   if (ws_bytes < wl.total) return STV_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -232,7 +236,7 @@ int stv_split_combine(const stv_shape* shape, const stv_seq* seqs, int n_seqs, i
   int sm = 0;
   if ((rc = device_sm_count(&sm))) return rc;
   Plan plan;
-  make_plan(sh, seqs, n_seqs, sm, &plan);
+  if ((rc = make_plan(sh, seqs, n_seqs, sm, &plan))) return rc;
   const WsLayout wl = ws_layout(sh, n_seqs, plan);
   if (ws_bytes < wl.total) return STV_ERR_WORKSPACE_TOO_SMALL;
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);

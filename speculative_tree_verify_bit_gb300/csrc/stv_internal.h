@@ -18,6 +18,7 @@ constexpr int kPageTok = 256;
 constexpr int kTileTok = 64;                 // V-code tiles and verify tiles
 constexpr int kMaxRows = 128;                // T * G per KV head
 constexpr int kMaxT = 32;
+constexpr int kMaxSplitsPerHead = 256;  // split_combine keeps one (m, l) per split in 8 registers x 32 lanes
 
 // Byte offsets inside one KV head's block of a page (see include/stv.h).
 constexpr int kOffKCodes = 0;

@@ -54,46 +54,71 @@ cudaError_t launch_quantize_q(const __half* q, int n_rows, int8_t* qi, float* sq
 }
 
 // ---------------------------------------------------------------------------
-// a5: split_combine.  One warp per (sequence, KV head, row); lane = 8 channels.
+// a5: split_combine.  One warp per (sequence, KV head, row, 64-channel
+// quarter); lane = 2 channels.  The warp reads a chunk of up to 32 splits'
+// (m, l) at once (split kb + j in lane j), forms M = max m and the weights
+// 2^(m - M), then issues the chunk's partial-O loads together (a fully
+// unrolled, predicated loop: one memory round trip per chunk rather than
+// one per split) and sums them in split order, so the result does not
+// depend on timing.
 
 __global__ void __launch_bounds__(256) split_combine_kernel(const __grid_constant__ CombineParams p) {
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int quarter = gw & 3, row_id = gw >> 2;
   int s = 0, base = 0;
-  while (s < p.n_seqs && gw >= base + p.hkv * p.R) {
+  while (s < p.n_seqs && row_id >= base + p.hkv * p.R) {
     base += p.hkv * p.R;
     ++s;
   }
   if (s >= p.n_seqs) return;
-  const int h = (gw - base) / p.R, r = (gw - base) % p.R;
+  const int h = (row_id - base) / p.R, r = (row_id - base) % p.R;
   const SeqDesc& sd = p.seq[s];
-  const int u0 = sd.unit_base + h * sd.splits;
+  const int u0 = sd.unit_base + h * sd.splits, splits = sd.splits;
+  const float2* ml = reinterpret_cast<const float2*>(p.ml);
+  // (m, l) of every split, 32 per register: at most kMaxChunks * 32 splits
+  constexpr int kMaxChunks = kMaxSplitsPerHead / 32;
+  float2 mlv[kMaxChunks];
   float M = -INFINITY;
-  for (int k = 0; k < sd.splits; ++k) M = fmaxf(M, p.ml[((int64_t)(u0 + k) * p.R + r) * 2]);
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, L = 0.f;
-  for (int k = 0; k < sd.splits; ++k) {
-    const int64_t at = (int64_t)(u0 + k) * p.R + r;
-    const float mk = p.ml[at * 2];
-    if (mk == -INFINITY) continue;
-    const float wk = exp2f(mk - M);
-    L += wk * p.ml[at * 2 + 1];
-    const float4* src = reinterpret_cast<const float4*>(p.o_part + at * kHeadDim + lane * 8);
-    const float4 a = src[0], b = src[1];
-    acc[0] += wk * a.x; acc[1] += wk * a.y; acc[2] += wk * a.z; acc[3] += wk * a.w;
-    acc[4] += wk * b.x; acc[5] += wk * b.y; acc[6] += wk * b.z; acc[7] += wk * b.w;
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  __align__(16) __half outv[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) outv[e] = __float2half_rn(acc[e] * inv);
+  for (int c = 0; c < kMaxChunks; ++c) {
+    const int k = c * 32 + lane;
+    mlv[c] = k < splits ? ml[(int64_t)(u0 + k) * p.R + r] : make_float2(-INFINITY, 0.f);
+    M = fmaxf(M, mlv[c].x);
+  }
+  M = wmax(M);
+  float L = 0.f, acc0 = 0.f, acc1 = 0.f;
+  const int64_t split_stride = (int64_t)p.R * kHeadDim;
+  const float* src = p.o_part + (int64_t)u0 * split_stride + (int64_t)r * kHeadDim + quarter * 64 + lane * 2;
+#pragma unroll 1
+  for (int c = 0; c < kMaxChunks && c * 32 < splits; ++c) {
+    const float w = mlv[0].x == -INFINITY ? 0.f : exp2f(mlv[0].x - M);
+    L += w * mlv[0].y;
+#pragma unroll
+    for (int i = 0; i + 1 < kMaxChunks; ++i) mlv[i] = mlv[i + 1];  // next chunk to [0], in registers
+    const int n = min(32, splits - c * 32);
+    const float* sp = src + (int64_t)(c * 32) * split_stride;
+    float2 o[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) o[j] = j < n ? *reinterpret_cast<const float2*>(sp + j * split_stride) : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float wk = __shfl_sync(0xffffffffu, w, j);
+      // a split with weight 0 (no visible key for this row) adds nothing
+      acc0 = wk != 0.f ? fmaf(wk, o[j].x, acc0) : acc0;
+      acc1 = wk != 0.f ? fmaf(wk, o[j].y, acc1) : acc1;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
   const int node = r / p.G, qh = h * p.G + r % p.G;
-  *reinterpret_cast<uint4*>(p.o + (((int64_t)s * p.T + node) * p.hq + qh) * kHeadDim + lane * 8) =
-      *reinterpret_cast<const uint4*>(outv);
+  *reinterpret_cast<__half2*>(p.o + (((int64_t)s * p.T + node) * p.hq + qh) * kHeadDim + quarter * 64 + lane * 2) =
+      __floats2half2_rn(acc0 * inv, acc1 * inv);
 }
 
 cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t s) {
-  int rows = 0;
-  for (int i = 0; i < p.n_seqs; ++i) rows += p.hkv * p.R;
-  split_combine_kernel<<<(rows + 7) / 8, 256, 0, s>>>(p);
+  const int warps = p.n_seqs * p.hkv * p.R * 4;  // four channel quarters per row
+  split_combine_kernel<<<(warps + 7) / 8, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

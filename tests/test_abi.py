@@ -82,6 +82,20 @@ def test_workspace_units_never_exceed_sm_count(lib):
         assert rc1 == 0 and rc2 == 0 and big >= small
 
 
+def test_split_plan_caps_splits_per_head(lib):
+    # 2^20 + 16 keys = 16,385 tiles per KV head.  Planned for 10,000 SMs the
+    # plan would cut them finer than the 256 splits split_combine accepts, so
+    # it takes ceil(16,385 / 256) = 65 tiles per split: 253 splits per head,
+    # 1,012 work units.
+    ctx = 1 << 20
+    rc, nbytes = _ws(stv.make_shape(), [ctx], [-(-(ctx + 16) // 256)], 16, 10_000)
+    assert rc == 0
+    units = 4 * -(-16385 // 65)
+    a = lambda x: (x + 255) // 256 * 256
+    assert units == 1012
+    assert nbytes == a(a(a(16 * 24 * 256) + 16 * 24 * 4) + units * 96 * 256 * 4) + units * 96 * 2 * 4
+
+
 @pytest.mark.parametrize("ctxs,pages,t,rc", [
     ([100], [1], 16, stv.STV_OK),
     ([250], [1], 16, stv.STV_ERR_INVALID_ARG),    # ctx + T past the pages
