@@ -180,12 +180,14 @@ class ClockSampler:
 class GpuRound:
     """All layers of one workload resident on the GPU, plus one round's inputs."""
 
-    def __init__(self, w: workloads.Workload, p_accept: float, device, layers: int | None = None):
+    def __init__(self, w: workloads.Workload, p_accept: float, device, layers: int | None = None,
+                 fuse_append: bool = False):
         import torch
 
         import speculative_tree_verify_bit_gb300 as stv
 
         self.stv, self.torch, self.w, self.dev = stv, torch, w, device
+        self.fuse_append = fuse_append
         self.L = layers or w.layers
         self.T, self.hq, self.hkv = w.t_nodes, w.hq, w.hkv
         self.shape = stv.make_shape(self.hq, self.hkv)
@@ -227,17 +229,23 @@ class GpuRound:
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
 
     def launches_per_step(self, path):
-        return self.L * (3 + (1 if path == "int8" else 0)) + 2
+        per_layer = (2 if self.fuse_append else 3) + (1 if path == "int8" else 0)
+        return self.L * per_layer + 2
 
     def step(self, path, verify_events=None):
         stv = self.stv
         for l in range(self.L):
-            stv.stv_kv_append_pack(self.shape, self.layers[l], self.seqs, self.k_tree[l], self.v_tree[l],
-                                   self.row_seq, self.row_pos, dev_status=self.status)
+            if not self.fuse_append:
+                stv.stv_kv_append_pack(self.shape, self.layers[l], self.seqs, self.k_tree[l], self.v_tree[l],
+                                       self.row_seq, self.row_pos, dev_status=self.status)
             if verify_events is not None:
                 verify_events[l][0].record()
-            stv.stv_verify_attn(self.shape, self.layers[l], self.seqs, self.q[l], self.parent, self.T, path, self.ws,
-                                dev_status=self.status)
+            if self.fuse_append:  # the tree rows' append runs inside the verify launch
+                stv.stv_append_verify_attn(self.shape, self.layers[l], self.seqs, self.k_tree[l], self.v_tree[l],
+                                           self.q[l], self.parent, self.T, path, self.ws, dev_status=self.status)
+            else:
+                stv.stv_verify_attn(self.shape, self.layers[l], self.seqs, self.q[l], self.parent, self.T, path,
+                                    self.ws, dev_status=self.status)
             if verify_events is not None:
                 verify_events[l][1].record()
             stv.stv_split_combine(self.shape, self.seqs, self.T, self.ws, self.o)
@@ -270,7 +278,7 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(dev)
     w = workloads.WORKLOADS[args.workload]
     p_accept = args.p_accept if args.p_accept is not None else w.p_accept[-1 if args.workload == "long262k" else 0]
-    r = GpuRound(w, p_accept, dev, layers=args.layers)
+    r = GpuRound(w, p_accept, dev, layers=args.layers, fuse_append=args.fuse_append)
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -466,6 +474,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--oracle-rows", type=int, default=32)
     ap.add_argument("--layers", type=int, default=None, help="fewer layers (profiling captures only)")
+    ap.add_argument("--fuse-append", action="store_true",
+                    help="append the tree rows inside the verify launch (stv_append_verify_attn) instead of "
+                         "with their own launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -499,7 +510,8 @@ def main():
         "config": {"workload": w.name, "ctx": list(w.ctx), "t_nodes": w.t_nodes, "layers": args.layers or w.layers,
                    "hq": w.hq, "hkv": w.hkv, "head_dim": 256, "path": args.path, "p_accept": res["p_accept"],
                    "l2": "inputs larger than L2 (16 layers of packed KV)", "parallelism": f"replicas{world}",
-                   "timing": "median over steps of one CUDA-graph replay of the round, CUDA events"},
+                   "timing": "median over steps of one CUDA-graph replay of the round, CUDA events",
+                   "append": "fused into verify" if args.fuse_append else "separate launch"},
         "gbs_per_layer_round": res["round_gbs"],
         "bytes_per_layer_round": res["bytes_lr"],
         "verify_us_per_launch": res["v_us"],

@@ -165,6 +165,25 @@ int stv_verify_attn(const stv_shape* shape, const stv_layer_cache* layer, const 
                     int32_t* dev_status, stv_stream_t stream);
 
 /*
+ * a1 + a2..a4 in one launch (the round's append fused into verify): packs the
+ * round's T tree rows into the cache exactly as stv_kv_append_pack would (row
+ * i of sequence s at position ctx_s + i, every KV head, K and V), then runs
+ * stv_verify_attn over the cache that now holds them.  The work unit whose
+ * key range holds a tree row packs it, before its bulk copies read that tile,
+ * so the rows never need a launch of their own ("elpis" README, "Why fast":
+ * tree verify pipe, host check after launch; syv-ai README (mirror), CUDA
+ * graph notes: an uncaptured verify step is launch-bound).
+ *  k_tree, v_tree: device fp16 [n_seqs][T][hkv][256], caller-owned, read only.
+ *  All other arguments, the workspace and the results as in stv_verify_attn;
+ *  the cache bytes written equal those of stv_kv_append_pack on the same rows.
+ *  STV_ERR_INVALID_ARG when k_tree or v_tree is null; a page-table entry
+ *  outside the pool sets STV_DEV_BAD_PAGE and that row is not written.
+ */
+int stv_append_verify_attn(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs, int n_seqs,
+                           const void* k_tree, const void* v_tree, const void* q, const int32_t* parent, int t_nodes,
+                           int path, void* workspace, size_t ws_bytes, int32_t* dev_status, stv_stream_t stream);
+
+/*
  * a5 -- merge the split partials of the last stv_verify_attn on this
  * workspace: per row M = max_s m_s, O = sum_s 2^(m_s - M) O_s / sum_s
  * 2^(m_s - M) l_s, splits taken in a fixed order (deterministic).

@@ -42,7 +42,7 @@ HEAD_BLOCK_BYTES = 57344
 EXPORTS = (
     "stv_status_string", "stv_version", "stv_page_bytes", "stv_kv_append_pack", "stv_verify_workspace_bytes",
     "stv_verify_attn", "stv_split_combine", "stv_tree_accept", "stv_kv_commit", "stv_int8_qk_dots",
-    "stv_verify_attn_no_alloc",
+    "stv_verify_attn_no_alloc", "stv_append_verify_attn",
 )
 
 
@@ -96,6 +96,8 @@ def load() -> ctypes.CDLL:
         lib.stv_kv_commit.argtypes = [P, P, I, P, I, I, P, P, P, P, P]
         lib.stv_int8_qk_dots.restype = I
         lib.stv_int8_qk_dots.argtypes = [P, P, P, P, I, I32, I32, P, P, P]
+        lib.stv_append_verify_attn.restype = I
+        lib.stv_append_verify_attn.argtypes = [P, P, P, I, P, P, P, P, I, I, P, ctypes.c_size_t, P, P]
         lib.stv_verify_attn_no_alloc.restype = I
         lib.stv_verify_attn_no_alloc.argtypes = [P, P, P, I, P, P, I, I, P, P, P]
         _lib = lib
@@ -227,6 +229,23 @@ def stv_verify_attn(shape, layer: LayerCache, seqs, q, parent, t_nodes: int, pat
         ctypes.byref(shape), ctypes.byref(lc), arr, len(seqs), _ptr(q, torch.float16, "q"),
         _ptr(parent, torch.int32, "parent"), int(t_nodes), int(path), _ptr(workspace, name="workspace"),
         workspace.numel() * workspace.element_size(), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+
+
+def stv_append_verify_attn(shape, layer: LayerCache, seqs, k_tree, v_tree, q, parent, t_nodes: int, path, workspace,
+                           dev_status=None, stream=None):
+    """stv_kv_append_pack of the round's tree rows (k_tree, v_tree: fp16
+    [n_seqs][T][hkv][256], row i of sequence s at ctx_s + i) fused into
+    stv_verify_attn: one launch."""
+    import torch
+
+    lc = layer.c()
+    arr = _seq_array(seqs)
+    path = PATHS.get(path, path)
+    _check("stv_append_verify_attn", load().stv_append_verify_attn(
+        ctypes.byref(shape), ctypes.byref(lc), arr, len(seqs), _ptr(k_tree, torch.float16, "k_tree"),
+        _ptr(v_tree, torch.float16, "v_tree"), _ptr(q, torch.float16, "q"), _ptr(parent, torch.int32, "parent"),
+        int(t_nodes), int(path), _ptr(workspace, name="workspace"), workspace.numel() * workspace.element_size(),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
 
 
 def stv_split_combine(shape, seqs, t_nodes: int, workspace, o, stream=None):

@@ -180,9 +180,10 @@ int stv_verify_workspace_bytes(const stv_shape* shape, const stv_seq* seqs, int 
   return STV_OK;
 }
 
-int stv_verify_attn(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs, int n_seqs,
-                    const void* q, const int32_t* parent, int t_nodes, int path, void* workspace, size_t ws_bytes,
-                    int32_t* dev_status, stv_stream_t stream) {
+// stv_verify_attn, and stv_append_verify_attn when k_tree / v_tree are given.
+static int verify_common(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs, int n_seqs,
+                         const void* k_tree, const void* v_tree, const void* q, const int32_t* parent, int t_nodes,
+                         int path, void* workspace, size_t ws_bytes, int32_t* dev_status, stv_stream_t stream) {
   ShapeInfo sh;
   int rc = check_shape(shape, t_nodes, &sh);
   if (rc) return rc;
@@ -216,6 +217,8 @@ int stv_verify_attn(const stv_shape* shape, const stv_layer_cache* layer, const 
   p.sq = reinterpret_cast<const float*>(ws + wl.off_sq);
   p.o_part = reinterpret_cast<float*>(ws + wl.off_opart);
   p.ml = reinterpret_cast<float*>(ws + wl.off_ml);
+  p.k_tree = static_cast<const __half*>(k_tree);
+  p.v_tree = static_cast<const __half*>(v_tree);
   p.status = dev_status;
   cudaStream_t s = (cudaStream_t)stream;
   if (path == STV_PATH_INT8) {
@@ -224,6 +227,21 @@ int stv_verify_attn(const stv_shape* shape, const stv_layer_cache* layer, const 
     if (e != cudaSuccess) return STV_ERR_CUDA;
   }
   return to_status(launch_verify(p, s));
+}
+
+int stv_verify_attn(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs, int n_seqs,
+                    const void* q, const int32_t* parent, int t_nodes, int path, void* workspace, size_t ws_bytes,
+                    int32_t* dev_status, stv_stream_t stream) {
+  return verify_common(shape, layer, seqs, n_seqs, nullptr, nullptr, q, parent, t_nodes, path, workspace, ws_bytes,
+                       dev_status, stream);
+}
+
+int stv_append_verify_attn(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs, int n_seqs,
+                           const void* k_tree, const void* v_tree, const void* q, const int32_t* parent, int t_nodes,
+                           int path, void* workspace, size_t ws_bytes, int32_t* dev_status, stv_stream_t stream) {
+  if (!k_tree || !v_tree) return STV_ERR_INVALID_ARG;
+  return verify_common(shape, layer, seqs, n_seqs, k_tree, v_tree, q, parent, t_nodes, path, workspace, ws_bytes,
+                       dev_status, stream);
 }
 
 int stv_split_combine(const stv_shape* shape, const stv_seq* seqs, int n_seqs, int t_nodes, const void* workspace,

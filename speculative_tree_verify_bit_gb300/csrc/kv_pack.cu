@@ -2,12 +2,9 @@
 //
 // kv_append_pack quantizes fp16 K/V rows into the paged 3-bit cache ("elpis"
 // README, header table: 3-bit KV cache, 12 KiB per token over 16 layers).
-// One CTA per (row, KV head); thread = channel, warp = one 32-channel group,
-// so the group maximum is one warp reduction and a K block's three words are
-// three warp-wide OR reductions.  V codes are channel-major (a block holds one
-// channel's codes for 32 tokens), so each thread read-modify-writes the three
-// bits of its own channel with atomics (rows appended in the same launch may
-// share a V block; their bits are disjoint).
+// One CTA per (row, KV head); thread = channel, warp = one 32-channel group
+// (append_row_channel in stv_device.cuh, shared with the verify kernel, which
+// packs the round's tree rows itself in stv_append_verify_attn).
 //
 // kv_commit moves the accepted rows to ctx .. ctx + n_commit - 1 ("elpis"
 // README, "Why fast": commit the longest matching path + 1).  One CTA per
@@ -18,25 +15,9 @@
 
 namespace stv {
 
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
-}
-
-// 3-bit code of x for scale s (the quantizer of include/stv.h).  x / s is an
-// IEEE single division: a quotient of two fp16 values lands on a half-integer
-// only when it is one, so rounding it half-to-even matches the exact rule.
-__device__ __forceinline__ int quant_code(float x, float s) {
-  if (s == 0.f) return 4;
-  float r = rintf(__fdiv_rn(x, s)) + 4.f;
-  r = fminf(fmaxf(r, 0.f), 7.f);
-  return (int)r;
-}
-
 __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ AppendParams p) {
   const int row = blockIdx.x / p.hkv, h = blockIdx.x % p.hkv;
-  const int c = threadIdx.x, g = c >> 5, lane = c & 31;
+  const int c = threadIdx.x;
   const int s = __ldg(p.row_seq + row), pos = __ldg(p.row_pos + row);
   if (s < 0 || s >= p.n_seqs || pos < 0) {
     if (c == 0) report(p.status, STV_DEV_BAD_ROW);
@@ -48,49 +29,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ 
   const int slot = pos & (kPageTok - 1);
   const int64_t src = ((int64_t)row * p.hkv + h) * kHeadDim + c;
 
-  // ---- K: token-major blocks ----
-  {
-    float x = __half2float(p.k[src]);
-    __half sh = __float2half_rn(warp_max(fabsf(x)) * 0.25f);
-    int code = quant_code(x, __half2float(sh));
-    uint32_t mine[3] = {0u, 0u, 0u};
-#pragma unroll
-    for (int b = 0; b < 3; ++b) {
-      int wd, bt;
-      bit_place(lane, b, wd, bt);
-      if ((code >> b) & 1) mine[wd] |= 1u << bt;
-    }
-    uint32_t w0 = __reduce_or_sync(0xffffffffu, mine[0]);
-    uint32_t w1 = __reduce_or_sync(0xffffffffu, mine[1]);
-    uint32_t w2 = __reduce_or_sync(0xffffffffu, mine[2]);
-    if (lane == 0) {
-      uint32_t* wp = reinterpret_cast<uint32_t*>(hb + kOffKCodes + slot * 96 + g * 12);
-      wp[0] = w0;
-      wp[1] = w1;
-      wp[2] = w2;
-      *reinterpret_cast<__half*>(hb + kOffKScales + slot * 16 + g * 2) = sh;
-    }
-  }
-  // ---- V: channel-major blocks of 32 tokens ----
-  {
-    float x = __half2float(p.v[src]);
-    __half sh = __float2half_rn(warp_max(fabsf(x)) * 0.25f);
-    int code = quant_code(x, __half2float(sh));
-    const int tile = slot / kTileTok, within = slot % kTileTok;
-    uint32_t* wp = reinterpret_cast<uint32_t*>(hb + kOffVCodes + tile * kVTileCodeBytes + c * 24 + (within / 32) * 12);
-    const int i = within % 32;
-#pragma unroll
-    for (int b = 0; b < 3; ++b) {
-      int wd, bt;
-      bit_place(i, b, wd, bt);
-      if ((code >> b) & 1)
-        atomicOr(wp + wd, 1u << bt);
-      else
-        atomicAnd(wp + wd, ~(1u << bt));
-    }
-    if (lane == 0)
-      *reinterpret_cast<__half*>(hb + kOffVScales + tile * kVTileScaleBytes + g * (kTileTok * 2) + within * 2) = sh;
-  }
+  append_row_channel(__half2float(p.k[src]), __half2float(p.v[src]), hb, slot, c);
 }
 
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t s) {

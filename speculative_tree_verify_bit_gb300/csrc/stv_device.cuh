@@ -95,4 +95,114 @@ __device__ __forceinline__ void decode_block_raw(uint32_t w0, uint32_t w1, uint3
   decode_block_h2(w0, w1, w2, [&](int) { return one; }, out);
 }
 
+// ---------------------------------------------------------------------------
+// a1, the per-row quantizer and packer (kv_append_pack; also run inside the
+// verify kernel for the round's tree rows).
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+// 3-bit code of x for scale s (the quantizer of include/stv.h):
+// clamp(rne(x / s) + 4, 0, 7), exactly, without a division.  q = x * (1/s)
+// from the approximate reciprocal is within far less than 1/2 of x / s
+// (|x / s| <= 8 here), so c = rint(q) is rne(x / s) or next to it, and only
+// when x / s lies near a half-integer.  The residual d = x - c s is exact:
+// either c = 0 (d = x) or |x| >= s/2, and then x and c s (fp16 values times
+// integers of at most 4 bits) are a few binades apart, so d needs at most
+// about 15 significant bits.  d against +-s/2 (exact) settles the rounding,
+// ties to the even integer.  s = fp16(max|x| / 4) is a normal fp32 value or
+// zero, so the reciprocal's flush-to-zero mode never applies.
+__device__ __forceinline__ int quant_code(float x, float s) {
+  if (s == 0.f) return 4;
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  int c = __float2int_rn(x * r);
+  const float d = fmaf(-(float)c, s, x), hs = 0.5f * s;
+  const bool odd = (c & 1) != 0;
+  if (d > hs || (d == hs && odd)) c += 1;        // closer to c + 1, or a tie with odd c
+  else if (d < -hs || (d == -hs && odd)) c -= 1;  // closer to c - 1, or a tie with odd c
+  return min(max(c + 4, 0), 7);
+}
+
+// One channel of one (row, KV head): called by 256 threads, thread c =
+// channel, warp = one 32-channel group (all 32 lanes take part).  K: the
+// group maximum is a warp reduction, the block's three words are three
+// warp-wide OR reductions, written by lane 0 with the group's scale.  V: the
+// group's scale is written by lane 0 and this channel's code is returned; V
+// codes are channel-major (a block holds one channel's codes for 32 tokens),
+// so the caller places the code's three bits.
+__device__ __forceinline__ int append_row_k_vscale(float xk, float xv, uint8_t* hb, int slot, int c) {
+  const int g = c >> 5, lane = c & 31;
+  {
+    __half sh = __float2half_rn(warp_max(fabsf(xk)) * 0.25f);
+    int code = quant_code(xk, __half2float(sh));
+    uint32_t m0 = 0u, m1 = 0u, m2 = 0u;  // this lane's bits of the block's three words
+#pragma unroll
+    for (int b = 0; b < 3; ++b) {
+      int wd, bt;
+      bit_place(lane, b, wd, bt);
+      const uint32_t bit = ((code >> b) & 1) ? 1u << bt : 0u;
+      m0 |= wd == 0 ? bit : 0u;
+      m1 |= wd == 1 ? bit : 0u;
+      m2 |= wd == 2 ? bit : 0u;
+    }
+    uint32_t w0 = __reduce_or_sync(0xffffffffu, m0);
+    uint32_t w1 = __reduce_or_sync(0xffffffffu, m1);
+    uint32_t w2 = __reduce_or_sync(0xffffffffu, m2);
+    if (lane == 0) {
+      uint32_t* wp = reinterpret_cast<uint32_t*>(hb + kOffKCodes + slot * 96 + g * 12);
+      wp[0] = w0;
+      wp[1] = w1;
+      wp[2] = w2;
+      *reinterpret_cast<__half*>(hb + kOffKScales + slot * 16 + g * 2) = sh;
+    }
+  }
+  __half sh = __float2half_rn(warp_max(fabsf(xv)) * 0.25f);
+  const int tile = slot / kTileTok, within = slot % kTileTok;
+  if (lane == 0)
+    *reinterpret_cast<__half*>(hb + kOffVScales + tile * kVTileScaleBytes + g * (kTileTok * 2) + within * 2) = sh;
+  return quant_code(xv, __half2float(sh));
+}
+
+// Address of the three V words (one 32-token block of channel c) holding
+// slot's code, and the code's index in that block.
+__device__ __forceinline__ uint32_t* v_block_words(uint8_t* hb, int slot, int c, int* index) {
+  const int tile = slot / kTileTok, within = slot % kTileTok;
+  *index = within % 32;
+  return reinterpret_cast<uint32_t*>(hb + kOffVCodes + tile * kVTileCodeBytes + c * 24 + (within / 32) * 12);
+}
+
+// Replaces code `index` of a 32-code block held in three words.
+__device__ __forceinline__ void set_block_code(uint32_t& w0, uint32_t& w1, uint32_t& w2, int index, int code) {
+#pragma unroll
+  for (int b = 0; b < 3; ++b) {
+    int wd, bt;
+    bit_place(index, b, wd, bt);
+    const uint32_t m = 1u << bt, v = ((code >> b) & 1) ? m : 0u;
+    w0 = wd == 0 ? ((w0 & ~m) | v) : w0;
+    w1 = wd == 1 ? ((w1 & ~m) | v) : w1;
+    w2 = wd == 2 ? ((w2 & ~m) | v) : w2;
+  }
+}
+
+// a1 for one channel of one row, V bits by atomics: rows packed by other
+// threads or CTAs at the same time may share the V block (disjoint bits).
+__device__ __forceinline__ void append_row_channel(float xk, float xv, uint8_t* hb, int slot, int c) {
+  const int code = append_row_k_vscale(xk, xv, hb, slot, c);
+  int i;
+  uint32_t* wp = v_block_words(hb, slot, c, &i);
+#pragma unroll
+  for (int b = 0; b < 3; ++b) {
+    int wd, bt;
+    bit_place(i, b, wd, bt);
+    if ((code >> b) & 1)
+      atomicOr(wp + wd, 1u << bt);
+    else
+      atomicAnd(wp + wd, ~(1u << bt));
+  }
+}
+
 }  // namespace stv

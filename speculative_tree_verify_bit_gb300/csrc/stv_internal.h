@@ -76,6 +76,11 @@ struct VerifyParams {
   const float* sq;        // [n_seqs][T][hq]
   float* o_part;          // [n_units][R][256]
   float* ml;              // [n_units][R][2] (m in log2 units, l)
+  // Tree rows to pack into the cache before they are read (fused append), or
+  // null when they are already there: fp16 [n_seqs][T][hkv][256], row i of
+  // sequence s goes to position ctx_s + i.
+  const __half* k_tree;
+  const __half* v_tree;
   int32_t* status;
 };
 

@@ -60,6 +60,7 @@ struct Bars {
   uint64_t kd_full[2], kd_empty[2], vd_full[2], vd_empty[2];
   uint64_t s_full[2], p_full[2];
   uint64_t pv_done, q_ready, mma_done;
+  uint64_t tree_packed;  // the round's tree rows of this unit are in the cache (fused append)
   uint32_t tmem_base;
   int abort;
   uint32_t anc[kMaxT];
@@ -245,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
     mbar_init(&bars->pv_done, 1);
     mbar_init(&bars->q_ready, 4);
     mbar_init(&bars->mma_done, 1);
+    mbar_init(&bars->tree_packed, 8);
     bars->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -279,10 +281,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
     // =================== producer ===================
     if (lane == 0) {
       int issued = 0;
+      bool tree_ready = p.k_tree == nullptr;
       for (int i = 0; i < n_tiles; ++i) {
         const int st = i % kStages;
         if (!wait1(&bars->raw_empty[st], ((i / kStages) & 1) ^ 1, abort_flag)) break;
         const int key0 = tok0 + i * kTileTok;
+        // a tile holding tree keys is copied only after the unpack warps have
+        // packed them (their global writes are fenced for the async proxy)
+        if (!tree_ready && key0 + kTileTok > sd.ctx && key0 < sd.ctx + T) {
+          if (!wait1(&bars->tree_packed, 0, abort_flag)) break;
+          tree_ready = true;
+        }
         const int64_t lp = key0 >> 8;
         int32_t page = lp < sd.n_pages ? __ldg(sd.page_table + lp) : -1;
         if (page < 0 || page >= p.pool_pages) {
@@ -525,6 +534,74 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
     // 128-bit store phase land on 8 different swizzled 16-byte positions.
     const int kj = (ut >> 5) * 8 + (ut & 7), kcb = (ut >> 3) & 3;
     const int vch = ut;  // V: channel
+    // ---- fused append: the tree rows whose keys fall in this unit's range ----
+    // (a1 for KV head h; thread ut = channel, warp = 32-channel group, the
+    // quantizer and bit layout of append_row_k_vscale).  Consecutive rows
+    // (T <= 32) touch at most two pages and, for channel ut, at most two
+    // 32-token V blocks: both are looked up and loaded once, before the loop,
+    // held in registers and written back after it (this thread alone writes
+    // channel ut's bits of these rows in this launch; other units hold other
+    // tiles).  The loop is rolled (this code runs once per launch, its
+    // instructions come cold) and packs two rows per iteration so that their
+    // reduction chains overlap; row values are loaded four rows ahead.
+    if (p.k_tree != nullptr) {
+      const int i0 = max(0, tok0 - sd.ctx), i1 = min(T, tok1 - sd.ctx);
+      if (i0 < i1) {
+        uint8_t* pool = const_cast<uint8_t*>(p.pool);
+        const int64_t pos0 = (int64_t)sd.ctx + i0, pos1 = (int64_t)sd.ctx + i1 - 1;
+        uint8_t* hb0 = const_cast<uint8_t*>(
+            head_block(sd, pool, p.page_bytes, p.pool_pages, pos0, h, ut == 0 ? p.status : nullptr));
+        uint8_t* hb1 = (pos1 >> 8) == (pos0 >> 8)
+                           ? hb0
+                           : const_cast<uint8_t*>(head_block(sd, pool, p.page_bytes, p.pool_pages, pos1, h,
+                                                             ut == 0 ? p.status : nullptr));
+        const __half* krow = p.k_tree + (((int64_t)s * T + i0) * p.hkv + h) * kHeadDim + ut;
+        const __half* vrow = p.v_tree + (((int64_t)s * T + i0) * p.hkv + h) * kHeadDim + ut;
+        const int64_t row_stride = (int64_t)p.hkv * kHeadDim;
+        float qk[4], qv[4];  // rows i .. i+3
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          qk[j] = i0 + j < i1 ? __half2float(krow[(int64_t)j * row_stride]) : 0.f;
+          qv[j] = i0 + j < i1 ? __half2float(vrow[(int64_t)j * row_stride]) : 0.f;
+        }
+        // V blocks A (first row's) and B (last row's, if another one)
+        int ia, ib;
+        uint32_t* wa = hb0 ? v_block_words(hb0, (int)(pos0 & (kPageTok - 1)), ut, &ia) : nullptr;
+        uint32_t* wb = hb1 ? v_block_words(hb1, (int)(pos1 & (kPageTok - 1)), ut, &ib) : nullptr;
+        if (wb == wa) wb = nullptr;
+        uint32_t a0 = 0u, a1 = 0u, a2 = 0u, b0 = 0u, b1 = 0u, b2 = 0u;
+        if (wa) { a0 = wa[0]; a1 = wa[1]; a2 = wa[2]; }
+        if (wb) { b0 = wb[0]; b1 = wb[1]; b2 = wb[2]; }
+        const int64_t blk_a = pos0 >> 5;
+#pragma unroll 1
+        for (int i = i0; i < i1; i += 2) {
+          const bool two = i + 1 < i1;  // warp-uniform
+          const float xk0 = qk[0], xv0 = qv[0], xk1 = qk[1], xv1 = qv[1];
+          qk[0] = qk[2]; qv[0] = qv[2]; qk[1] = qk[3]; qv[1] = qv[3];
+          if (i + 4 < i1) { qk[2] = __half2float(krow[(int64_t)(i + 4 - i0) * row_stride]); qv[2] = __half2float(vrow[(int64_t)(i + 4 - i0) * row_stride]); }
+          if (i + 5 < i1) { qk[3] = __half2float(krow[(int64_t)(i + 5 - i0) * row_stride]); qv[3] = __half2float(vrow[(int64_t)(i + 5 - i0) * row_stride]); }
+          const int64_t pa = (int64_t)sd.ctx + i, pb = pa + 1;
+          uint8_t* ha = (pa >> 8) == (pos0 >> 8) ? hb0 : hb1;
+          uint8_t* hbb = (pb >> 8) == (pos0 >> 8) ? hb0 : hb1;
+          int ca = 0, cb = 0;
+          if (ha) ca = append_row_k_vscale(xk0, xv0, ha, (int)(pa & (kPageTok - 1)), ut);
+          if (two && hbb) cb = append_row_k_vscale(xk1, xv1, hbb, (int)(pb & (kPageTok - 1)), ut);
+          if (ha) {
+            if ((pa >> 5) == blk_a) set_block_code(a0, a1, a2, (int)(pa & 31), ca);
+            else set_block_code(b0, b1, b2, (int)(pa & 31), ca);
+          }
+          if (two && hbb) {
+            if ((pb >> 5) == blk_a) set_block_code(a0, a1, a2, (int)(pb & 31), cb);
+            else set_block_code(b0, b1, b2, (int)(pb & 31), cb);
+          }
+        }
+        if (wa) { wa[0] = a0; wa[1] = a1; wa[2] = a2; }
+        if (wb) { wb[0] = b0; wb[1] = b1; wb[2] = b2; }
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->tree_packed);
+      }
+    }
     for (int i = 0; i < n_tiles; ++i) {
       const int st = i % kStages, b = i & 1;
       const uint8_t* stage = ring + st * kStageBytes;

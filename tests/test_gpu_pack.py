@@ -84,3 +84,35 @@ def test_host_validation_rejects_before_launch(gpu):
     with pytest.raises(stv.StvError) as e:
         stv.stv_kv_append_pack(stv.make_shape(24, 4), stv.LayerCache.empty(1, 2, device=gpu), seqs, k, k, idx, idx)
     assert e.value.status == stv.STV_ERR_SHAPE_UNSUPPORTED
+
+
+@pytest.mark.parametrize("m", [4.0, 3.0, 0.37, 1000.0, 65504.0, 6.0e-5, 5 * 2.0 ** -24, 7 * 2.0 ** -24])
+def test_pack_quantizer_every_fp16_value(gpu, m):
+    """Every finite fp16 value in [-m, m] quantized in a group whose maximum
+    is m (channel 0 of each group holds m), as K and as V: the cache bytes
+    equal the oracle's.  The scales include fp16-subnormal ones (the last two
+    maxima give s = 2^-24 and 2^-23, where x / s reaches 5 and 3.5)."""
+    h = np.arange(65536, dtype=np.uint16).view(np.float16)
+    vals = h[np.isfinite(h) & (np.abs(h.astype(np.float64)) <= np.float16(m))]
+    n_groups = -(-len(vals) // 31)
+    groups = np.zeros((n_groups, 32), np.float16)
+    groups[:, 0] = np.float16(m)
+    flat = groups[:, 1:].reshape(-1)
+    flat[:len(vals)] = vals
+    groups[:, 1:] = flat.reshape(n_groups, 31)
+    n_rows = -(-n_groups // 8)
+    rows = np.zeros((n_rows * 8, 32), np.float16)
+    rows[:n_groups] = groups
+    rows = rows.reshape(n_rows, 1, 256)
+    pages = -(-n_rows // 256)
+    table = np.arange(pages, dtype=np.int32)
+    pos = np.arange(n_rows, dtype=np.int32)
+    vrows = (-rows).copy()
+    layer = stv.LayerCache.empty(pages, 1, device=gpu)
+    seqs = [stv.Seq(torch.as_tensor(table, device=gpu), 0)]
+    stv.stv_kv_append_pack(stv.make_shape(1, 1), layer, seqs, torch.as_tensor(rows, device=gpu),
+                           torch.as_tensor(vrows, device=gpu), torch.zeros(n_rows, dtype=torch.int32, device=gpu),
+                           torch.as_tensor(pos, device=gpu))
+    cache = oracle.Cache(1, pages)
+    oracle.kv_append(cache, [table], rows, vrows, np.zeros(n_rows, np.int32), pos)
+    assert np.array_equal(layer.pool.cpu().numpy(), cache.pool)
