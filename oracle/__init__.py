@@ -83,6 +83,8 @@ def _load():
             lib.orc_kv_commit.argtypes = [P, I64, I32, I32, P, P, P, I, P, P, I]
             lib.orc_decode_rows.restype = I
             lib.orc_decode_rows.argtypes = [P, I64, I32, I32, P, P, I, I64, I64, I, P]
+            lib.orc_lookup_draft.restype = I
+            lib.orc_lookup_draft.argtypes = [P, I64, I, I, I, P, P, P, P]
             _lib = lib
     return _lib
 
@@ -286,3 +288,19 @@ def kv_commit(cache: Cache, page_tables, ctx, n_commit, path, t: int):
                               _p(c), len(c), _p(n), _p(pth), int(t)),
         "kv_commit",
     )
+
+
+def lookup_draft(history, min_len: int = 6, max_len: int = 12, k: int = 15):
+    """Lookup drafting (stv_oracle.c, orc_lookup_draft): propose the up to k
+    tokens that followed the latest earlier occurrence of the history's
+    longest suffix of length max_len .. min_len.  Returns
+    (proposal int32 array, match_len, match_pos); match_len 0 and match_pos -1
+    when no suffix of those lengths occurs earlier."""
+    h = np.ascontiguousarray(history, dtype=np.int32)
+    prop = np.zeros(max(k, 1), np.int32)
+    n_prop, mlen, mpos = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64()
+    rc = _load().orc_lookup_draft(_p(h), len(h), int(min_len), int(max_len), int(k), ctypes.byref(n_prop), _p(prop),
+                                  ctypes.byref(mlen), ctypes.byref(mpos))
+    if rc != 0:
+        raise ValueError("orc_lookup_draft: bad lengths")
+    return prop[:n_prop.value].copy(), mlen.value, mpos.value

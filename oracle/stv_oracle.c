@@ -642,3 +642,46 @@ int orc_decode_rows(const uint8_t* pool, int64_t page_bytes, int32_t pool_pages,
     }
   return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------
+ * Lookup drafting.  Reddit posts (u/iamMess), "Now added" list, lookup-
+ * augmented drafting: one kernel scans the request's own token history for
+ * the most recent occurrence of the last 6-12 generated tokens and proposes
+ * the tokens that followed it; syv-ai README (mirror), SPEC=dflash2 section:
+ * verify positions beyond the drafter's are filled from the request's own
+ * context.
+ *
+ * Reading (the pages do not say which of 6..12 wins): lengths are tried from
+ * the longest (max_len) down to the shortest (min_len); for the first length
+ * L whose suffix h[n-L .. n-1] occurs earlier, at a start p < n - L (the
+ * occurrence may overlap the suffix), the latest such p is taken and up to k
+ * tokens h[p+L .. ] are proposed, never past the end of the history.  With no
+ * occurrence at any length nothing is proposed (match_len 0, match_pos -1).
+ * Written as that definition: every length, every start, every token
+ * compared.
+ */
+int orc_lookup_draft(const int32_t* h, int64_t n, int min_len, int max_len, int k, int32_t* n_prop, int32_t* prop,
+                     int32_t* match_len, int64_t* match_pos) {
+  if (min_len < 1 || max_len < min_len || k < 0) return -1;
+  *n_prop = 0;
+  *match_len = 0;
+  *match_pos = -1;
+  for (int L = max_len; L >= min_len; --L) {
+    if ((int64_t)L >= n) continue;  /* the suffix needs an earlier start */
+    for (int64_t p = n - L - 1; p >= 0; --p) {
+      int same = 1;
+      for (int i = 0; i < L; ++i)
+        if (h[p + i] != h[n - L + i]) { same = 0; break; }
+      if (same) {
+        int64_t avail = n - (p + L);
+        int cnt = (int)(avail < k ? avail : k);
+        for (int j = 0; j < cnt; ++j) prop[j] = h[p + L + j];
+        *n_prop = cnt;
+        *match_len = L;
+        *match_pos = p;
+        return 0;
+      }
+    }
+  }
+  return 0;
+}
