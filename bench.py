@@ -271,6 +271,42 @@ def e2e_step(r: GpuRound, host, path):
     host["out_ids"].copy_(r.out_ids, non_blocking=True)
 
 
+def measure_lookup(w: workloads.Workload, dev, reps: int = 50, min_len: int = 6, max_len: int = 12, k: int = 15):
+    """Lookup drafting (stv_lookup_draft) over one history per request of
+    the workload, as long as its context (quoted spans planted with p = 0.7).
+    L2 is flushed before every timed call (the histories alone would fit in
+    L2); CUDA events around each call.  Bytes = 4 per history token."""
+    import torch
+
+    import speculative_tree_verify_bit_gb300 as stv
+
+    hs = [torch.as_tensor(h, device=dev) for h in workloads.lookup_histories(w)]
+    n = len(hs)
+    n_prop = torch.zeros(n, dtype=torch.int32, device=dev)
+    prop = torch.zeros((n, k), dtype=torch.int32, device=dev)
+    mlen = torch.zeros(n, dtype=torch.int32, device=dev)
+    mpos = torch.zeros(n, dtype=torch.int64, device=dev)
+    ws = torch.empty(stv.stv_lookup_workspace_bytes(n), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    times = []
+    for i in range(reps + 3):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        stv.stv_lookup_draft(hs, min_len, max_len, k, n_prop, prop, mlen, mpos, ws)
+        b.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            times.append(a.elapsed_time(b) * 1e3)
+    us = statistics.median(times)
+    nbytes = 4 * sum(h.numel() for h in hs)
+    peak, kind = measured_peak()
+    return {"us_per_call": us, "requests": n, "history_tokens": sum(h.numel() for h in hs), "k": k,
+            "min_len": min_len, "max_len": max_len, "bytes": nbytes, "gbs": nbytes / (us * 1e-6) / 1e9,
+            "frac": nbytes / (us * 1e-6) / 1e9 / peak, "peak_source": kind, "l2": "flushed before each call",
+            "proposed": int(n_prop.sum().item())}
+
+
 def run_gpu(args, rank, world):
     import torch
 
@@ -359,6 +395,7 @@ def run_gpu(args, rank, world):
     e2e_ms = e0.elapsed_time(e1)
 
     med_ms = statistics.median(round_ms)  # a round = one graph replay
+    lookup = measure_lookup(w, dev) if rank == 0 else None
     times = torch.tensor([med_ms, e2e_ms], device=dev)
     if dist is not None:
         dist.all_reduce(times, op=dist.ReduceOp.MAX)
@@ -375,7 +412,8 @@ def run_gpu(args, rank, world):
     return dict(rank=rank, us_per_lr=us_per_lr, e2e_us=e2e_us, bytes_lr=bytes_lr, v_us=v_us, vbytes=vbytes,
                 peak=peak, peak_kind=peak_kind, achieved=achieved, clocks=clk.summary(), status=st, h2d=h2d,
                 d2h=d2h, launches=r.launches_per_step(args.path) * args.steps, p_accept=p_accept, traffic=traffic,
-                n_units=None, ws_bytes=r.ws_bytes, round_gbs=bytes_lr / (us_per_lr * 1e-6) / 1e9 / world)
+                n_units=None, ws_bytes=r.ws_bytes, round_gbs=bytes_lr / (us_per_lr * 1e-6) / 1e9 / world,
+                lookup=lookup)
 
 
 def load_traffic(workload, path):
@@ -524,6 +562,7 @@ def main():
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
         "dev_status": res["status"],
+        "next_rows": {"lookup_draft": res.get("lookup")},
     }
     print(json.dumps(line), flush=True)
 

@@ -258,6 +258,41 @@ int stv_verify_attn_no_alloc(const stv_shape* shape, const stv_layer_cache* laye
                              const void* q, const int32_t* parent, int t_nodes, int path, void* o,
                              int32_t* dev_status, stv_stream_t stream);
 
+/*
+ * Lookup drafting (next row f4).  Reddit posts (u/iamMess), "Now added" list,
+ * lookup-augmented drafting: scan the request's own token history for the
+ * most recent occurrence of its last 6-12 tokens and propose the tokens that
+ * followed; syv-ai README (mirror), SPEC=dflash2 section: verify positions
+ * beyond the drafter's are filled from the request's own context.
+ *
+ * For each sequence with history h[0 .. n-1]: lengths L = max_len down to
+ * min_len are tried; for the first L whose suffix h[n-L .. n-1] occurs at an
+ * earlier start p < n - L (the occurrence may overlap the suffix), the
+ * latest such p is taken and up to k tokens h[p+L ..] are proposed, never
+ * past h[n-1].  With no occurrence nothing is proposed.
+ *  hist:      host array of n_seqs descriptors; each tokens pointer is device
+ *             int32 [n] owned by the caller (read only); n may be 0.
+ *  min_len, max_len: 1 <= min_len <= max_len <= 32.   k: 0 <= k <= 64.
+ *  n_prop:    device int32 [n_seqs]: tokens proposed (0..k).
+ *  prop:      device int32 [n_seqs][k]: the proposal, zero beyond n_prop.
+ *  match_len: device int32 [n_seqs]: L, or 0 when nothing matched.
+ *  match_pos: device int64 [n_seqs]: p, or -1 when nothing matched.
+ *  workspace: device, at least stv_lookup_workspace_bytes(n_seqs) bytes;
+ *             caller-owned scratch, contents need not be preserved.
+ * Returns STV_ERR_INVALID_ARG for lengths, k or n_seqs out of range, null
+ * pointers or a workspace too small (STV_ERR_WORKSPACE_TOO_SMALL).  The
+ * result is unique, so it does not depend on timing.
+ */
+typedef struct {
+  const int32_t* tokens;
+  int64_t n;
+} stv_history;
+
+int stv_lookup_workspace_bytes(int n_seqs, size_t* bytes);
+int stv_lookup_draft(const stv_history* hist, int n_seqs, int min_len, int max_len, int k, int32_t* n_prop,
+                     int32_t* prop, int32_t* match_len, int64_t* match_pos, void* workspace, size_t ws_bytes,
+                     stv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -42,7 +42,7 @@ HEAD_BLOCK_BYTES = 57344
 EXPORTS = (
     "stv_status_string", "stv_version", "stv_page_bytes", "stv_kv_append_pack", "stv_verify_workspace_bytes",
     "stv_verify_attn", "stv_split_combine", "stv_tree_accept", "stv_kv_commit", "stv_int8_qk_dots",
-    "stv_verify_attn_no_alloc", "stv_append_verify_attn",
+    "stv_verify_attn_no_alloc", "stv_append_verify_attn", "stv_lookup_workspace_bytes", "stv_lookup_draft",
 )
 
 
@@ -59,6 +59,10 @@ class stv_shape(ctypes.Structure):
 
 class stv_layer_cache(ctypes.Structure):
     _fields_ = [("pool", ctypes.c_void_p), ("page_bytes", ctypes.c_int64), ("n_pages", ctypes.c_int32)]
+
+
+class stv_history(ctypes.Structure):
+    _fields_ = [("tokens", ctypes.c_void_p), ("n", ctypes.c_int64)]
 
 
 class stv_seq(ctypes.Structure):
@@ -96,6 +100,10 @@ def load() -> ctypes.CDLL:
         lib.stv_kv_commit.argtypes = [P, P, I, P, I, I, P, P, P, P, P]
         lib.stv_int8_qk_dots.restype = I
         lib.stv_int8_qk_dots.argtypes = [P, P, P, P, I, I32, I32, P, P, P]
+        lib.stv_lookup_workspace_bytes.restype = I
+        lib.stv_lookup_workspace_bytes.argtypes = [I, P]
+        lib.stv_lookup_draft.restype = I
+        lib.stv_lookup_draft.argtypes = [P, I, I, I, I, P, P, P, P, P, ctypes.c_size_t, P]
         lib.stv_append_verify_attn.restype = I
         lib.stv_append_verify_attn.argtypes = [P, P, P, I, P, P, P, P, I, I, P, ctypes.c_size_t, P, P]
         lib.stv_verify_attn_no_alloc.restype = I
@@ -306,3 +314,27 @@ def stv_verify_attn_no_alloc(shape, layer: LayerCache, seqs, q, parent, t_nodes:
         ctypes.byref(shape), ctypes.byref(lc), arr, len(seqs), _ptr(q, torch.float16, "q"),
         _ptr(parent, torch.int32, "parent"), int(t_nodes), int(path), _ptr(o, torch.float16, "o"),
         _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+
+
+def stv_lookup_workspace_bytes(n_seqs: int) -> int:
+    out = ctypes.c_size_t()
+    _check("stv_lookup_workspace_bytes", load().stv_lookup_workspace_bytes(int(n_seqs), ctypes.byref(out)))
+    return out.value
+
+
+def stv_lookup_draft(histories, min_len: int, max_len: int, k: int, n_prop, prop, match_len, match_pos, workspace,
+                     stream=None):
+    """Lookup drafting over each history (int32 CUDA tensors): the up to k
+    tokens that followed the latest earlier occurrence of the longest suffix
+    of length max_len .. min_len (include/stv.h)."""
+    import torch
+
+    arr = (stv_history * len(histories))()
+    for i, t in enumerate(histories):
+        arr[i].tokens = _ptr(t, torch.int32, "history").value if t.numel() else None
+        arr[i].n = t.numel()
+    _check("stv_lookup_draft", load().stv_lookup_draft(
+        arr, len(histories), int(min_len), int(max_len), int(k), _ptr(n_prop, torch.int32, "n_prop"),
+        _ptr(prop, torch.int32, "prop"), _ptr(match_len, torch.int32, "match_len"),
+        _ptr(match_pos, torch.int64, "match_pos"), _ptr(workspace, name="workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream)))

@@ -212,3 +212,21 @@ def round_trees(w: Workload, p: float | None = None) -> RoundInputs:
         dr.append(d)
         am.append(a)
     return RoundInputs(np.stack(par), np.stack(dr), np.stack(am))
+
+
+def token_history(seed: int, n: int, p_copy: float = 0.7, tail: int = 64, alphabet: int = VOCAB) -> np.ndarray:
+    """Seeded synthetic token history of n ids for lookup drafting: uniform
+    ids over `alphabet`; with probability p_copy its last `tail` tokens repeat
+    an earlier span, as when an answer quotes its prompt ("reproduce every
+    command" work).  Random draws only."""
+    rng = np.random.default_rng(seed)
+    h = rng.integers(0, alphabet, n, dtype=np.int64).astype(np.int32)
+    if n > 2 * tail and rng.random() < p_copy:
+        a = int(rng.integers(0, n - 2 * tail))
+        h[n - tail:] = h[a:a + tail]
+    return h
+
+
+def lookup_histories(w: Workload, p_copy: float = 0.7):
+    """One history per request of the workload, as long as its context."""
+    return [token_history(1000 + 31 * s + w.ctx[s] % 997, c, p_copy) for s, c in enumerate(w.ctx)]
