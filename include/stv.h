@@ -260,10 +260,11 @@ int stv_verify_attn_no_alloc(const stv_shape* shape, const stv_layer_cache* laye
 
 /*
  * Lookup drafting (next row f4).  Reddit posts (u/iamMess), "Now added" list,
- * lookup-augmented drafting: scan the request's own token history for the
- * most recent occurrence of its last 6-12 tokens and propose the tokens that
- * followed; syv-ai README (mirror), SPEC=dflash2 section: verify positions
- * beyond the drafter's are filled from the request's own context.
+ * lookup-augmented drafting (draft tokens copied from earlier in the same
+ * request: find where its trailing tokens, between six and twelve of them,
+ * last appeared before, and take what came next); syv-ai README (mirror),
+ * SPEC=dflash2 section (verify slots past the drafter's come from the
+ * request's own context).
  *
  * For each sequence with history h[0 .. n-1]: lengths L = max_len down to
  * min_len are tried; for the first L whose suffix h[n-L .. n-1] occurs at an

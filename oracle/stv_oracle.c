@@ -645,11 +645,10 @@ int orc_decode_rows(const uint8_t* pool, int64_t page_bytes, int32_t pool_pages,
 
 /* ------------------------------------------------------------------------
  * Lookup drafting.  Reddit posts (u/iamMess), "Now added" list, lookup-
- * augmented drafting: one kernel scans the request's own token history for
- * the most recent occurrence of the last 6-12 generated tokens and proposes
- * the tokens that followed it; syv-ai README (mirror), SPEC=dflash2 section:
- * verify positions beyond the drafter's are filled from the request's own
- * context.
+ * augmented drafting: draft tokens are copied from earlier in the same
+ * request, from where its trailing tokens (six to twelve of them) last
+ * appeared before; syv-ai README (mirror), SPEC=dflash2 section: verify slots
+ * past the drafter's come from the request's own context.
  *
  * Reading (the pages do not say which of 6..12 wins): lengths are tried from
  * the longest (max_len) down to the shortest (min_len); for the first length

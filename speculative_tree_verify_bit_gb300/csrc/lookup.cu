@@ -3,10 +3,10 @@
 // max_len .. min_len tokens.
 //
 // Sources: Reddit posts (u/iamMess), "Now added" list, lookup-augmented
-// drafting (one kernel scans the request's own token history for the most
-// recent occurrence of the last 6-12 generated tokens and proposes what
-// followed); syv-ai README (mirror), SPEC=dflash2 section (verify positions
-// past the drafter's are filled from the request's own context).
+// drafting (draft tokens copied from earlier in the same request, where its
+// trailing six to twelve tokens last appeared); syv-ai README (mirror),
+// SPEC=dflash2 section (verify slots past the drafter's come from the
+// request's own context).
 //
 // One pass over the history.  A candidate is the END position e of an
 // earlier occurrence (e <= n - 2); its backward match length is
@@ -17,8 +17,9 @@
 // (plus max_len - 1 tokens to its left) in shared memory with coalesced
 // loads, reduces its chunk, and folds the result into the sequence's key
 // with a 64-bit atomicMax.  The last CTA of a sequence to finish (a done
-// counter; no CTA ever waits for another) writes the proposal.  The scan is
-// bound by HBM: 4 bytes of history per token.
+// counter; no CTA ever waits for another) writes the proposal.  It reads
+// 4 bytes of history per token; at one request's history (a megabyte at 262K
+// tokens) the call is bound by launch and load latency rather than bandwidth.
 #include <stdint.h>
 #include <string.h>
 

@@ -1,6 +1,6 @@
 """Pins for the lookup-drafting oracle (Reddit posts (u/iamMess), "Now added"
-list, lookup-augmented drafting: propose what followed the most recent
-earlier occurrence of the last 6-12 tokens).
+list, lookup-augmented drafting: draft tokens copied from where the request's
+trailing six to twelve tokens last appeared earlier in it).
 
 The oracle tries every length from longest to shortest and every start, token
 by token.  Here it is checked against hand-worked cases and against a search
