@@ -307,13 +307,30 @@ def measure_lookup(w: workloads.Workload, dev, reps: int = 50, min_len: int = 6,
             "proposed": int(n_prop.sum().item())}
 
 
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Each value's maximum over all ranks (the slowest replica sets the
+    job's time); unchanged on one process."""
+    import torch
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def us_per_layer_round(round_ms: float, layers: int, world: int) -> float:
+    """Whole-job value: N replicas each complete `layers` layer-rounds in the
+    slowest rank's round time, so the job does N x layers of them."""
+    return round_ms * 1e3 / (layers * world)
+
+
 def run_gpu(args, rank, world):
     import torch
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     w = workloads.WORKLOADS[args.workload]
-    p_accept = args.p_accept if args.p_accept is not None else w.p_accept[-1 if args.workload == "long262k" else 0]
+    p_accept = default_p_accept(args, w)
     r = GpuRound(w, p_accept, dev, layers=args.layers, fuse_append=args.fuse_append)
     dist = None
     if world > 1:
@@ -396,12 +413,9 @@ def run_gpu(args, rank, world):
 
     med_ms = statistics.median(round_ms)  # a round = one graph replay
     lookup = measure_lookup(w, dev) if rank == 0 else None
-    times = torch.tensor([med_ms, e2e_ms], device=dev)
-    if dist is not None:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    med_ms, e2e_ms = float(times[0]), float(times[1])
+    med_ms, e2e_ms = max_over_ranks([med_ms, e2e_ms], dist, dev)
     layer_rounds = args.steps * r.L * world
-    us_per_lr = med_ms * 1e3 / (r.L * world)
+    us_per_lr = us_per_layer_round(med_ms, r.L, world)
     e2e_us = e2e_ms * 1e3 / layer_rounds
     bytes_lr = algorithmic_bytes_per_layer_round(w.ctx, w.t_nodes, w.hq, w.hkv)
     vbytes = verify_kernel_bytes(w.ctx, w.t_nodes, w.hq, w.hkv)
@@ -474,6 +488,19 @@ def oracle_sample(w: workloads.Workload, n_rows: int, threads: int):
     return us_per_lr, dt, sample
 
 
+def arm_config(args, w: workloads.Workload, p_accept: float, world: int) -> dict:
+    """The workload both arms (the GPU path and the oracle) report."""
+    return {"workload": w.name, "ctx": list(w.ctx), "t_nodes": w.t_nodes, "layers": args.layers or w.layers,
+            "hq": w.hq, "hkv": w.hkv, "head_dim": 256, "path": args.path, "p_accept": p_accept,
+            "l2": "inputs larger than L2 (16 layers of packed KV)", "parallelism": f"replicas{world}",
+            "timing": "median over steps of one CUDA-graph replay of the round, CUDA events",
+            "append": "fused into verify" if args.fuse_append else "separate launch"}
+
+
+def default_p_accept(args, w: workloads.Workload) -> float:
+    return args.p_accept if args.p_accept is not None else w.p_accept[-1 if args.workload == "long262k" else 0]
+
+
 def run_reference(args):
     w = workloads.WORKLOADS[args.workload]
     threads = os.cpu_count() or 1
@@ -491,8 +518,7 @@ def run_reference(args):
         "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus, "steps": len(vals),
         "warmup": args.warmup, "ms_per_step": val * w.layers / 1e3, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": {"workload": w.name, "ctx": list(w.ctx), "t_nodes": w.t_nodes, "layers": w.layers, "hq": w.hq,
-                   "hkv": w.hkv, "head_dim": 256},
+        "config": arm_config(args, w, default_p_accept(args, w), 1),
         "cpu_baseline": {"value": val, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -545,11 +571,7 @@ def main():
         "metric": METRIC, "value": res["us_per_lr"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["us_per_lr"] * (args.layers or w.layers) * world / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": w.name, "ctx": list(w.ctx), "t_nodes": w.t_nodes, "layers": args.layers or w.layers,
-                   "hq": w.hq, "hkv": w.hkv, "head_dim": 256, "path": args.path, "p_accept": res["p_accept"],
-                   "l2": "inputs larger than L2 (16 layers of packed KV)", "parallelism": f"replicas{world}",
-                   "timing": "median over steps of one CUDA-graph replay of the round, CUDA events",
-                   "append": "fused into verify" if args.fuse_append else "separate launch"},
+        "config": arm_config(args, w, res["p_accept"], world),
         "gbs_per_layer_round": res["round_gbs"],
         "bytes_per_layer_round": res["bytes_lr"],
         "verify_us_per_launch": res["v_us"],
