@@ -259,6 +259,30 @@ int stv_verify_attn_no_alloc(const stv_shape* shape, const stv_layer_cache* laye
                              int32_t* dev_status, stv_stream_t stream);
 
 /*
+ * Prefill attention over the 3-bit cache (next row f2): every token of a
+ * prompt attends causally to the cache and to the prompt tokens before it.
+ * "elpis" README, "Why fast" (prefill int8 Q.K^T, 3021c; prefill K/V
+ * double-buffered ring, 3022: the next tile loads while the current one is
+ * computed).  Built on the verify kernel: a chunk of C consecutive prompt
+ * tokens is a chain tree (parent[i] = i - 1), whose ancestor-or-self mask is
+ * the causal mask, appended after the tokens before it; C = min(32,
+ * floor(128 / (hq / hkv))) rows per chunk fill the 128-row tile; up to 64
+ * chunks run in one verify launch, then the split merge.
+ *  seq:      ctx = tokens cached before the prompt; the prompt's own K/V
+ *            rows must already be in the cache at ctx .. ctx + n_tokens - 1
+ *            (stv_kv_append_pack), so attention reads them in 3-bit, like
+ *            every cached token.
+ *  q:        device fp16 [n_tokens][hq][256].   o: device fp16 [n_tokens][hq][256].
+ *  path:     STV_PATH_EXACT or STV_PATH_INT8, as in stv_verify_attn.
+ *  workspace: device, at least stv_prefill_workspace_bytes(...) bytes.
+ * Errors as in stv_verify_attn; n_tokens < 1 is STV_ERR_INVALID_ARG.
+ */
+int stv_prefill_workspace_bytes(const stv_shape* shape, const stv_seq* seq, int n_tokens, size_t* bytes);
+int stv_prefill_attn(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seq, const void* q,
+                     int n_tokens, int path, void* workspace, size_t ws_bytes, void* o, int32_t* dev_status,
+                     stv_stream_t stream);
+
+/*
  * Lookup drafting (next row f4).  Reddit posts (u/iamMess), "Now added" list,
  * lookup-augmented drafting (draft tokens copied from earlier in the same
  * request: find where its trailing tokens, between six and twelve of them,

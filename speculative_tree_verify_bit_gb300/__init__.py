@@ -43,6 +43,7 @@ EXPORTS = (
     "stv_status_string", "stv_version", "stv_page_bytes", "stv_kv_append_pack", "stv_verify_workspace_bytes",
     "stv_verify_attn", "stv_split_combine", "stv_tree_accept", "stv_kv_commit", "stv_int8_qk_dots",
     "stv_verify_attn_no_alloc", "stv_append_verify_attn", "stv_lookup_workspace_bytes", "stv_lookup_draft",
+    "stv_prefill_workspace_bytes", "stv_prefill_attn",
 )
 
 
@@ -100,6 +101,10 @@ def load() -> ctypes.CDLL:
         lib.stv_kv_commit.argtypes = [P, P, I, P, I, I, P, P, P, P, P]
         lib.stv_int8_qk_dots.restype = I
         lib.stv_int8_qk_dots.argtypes = [P, P, P, P, I, I32, I32, P, P, P]
+        lib.stv_prefill_workspace_bytes.restype = I
+        lib.stv_prefill_workspace_bytes.argtypes = [P, P, I, P]
+        lib.stv_prefill_attn.restype = I
+        lib.stv_prefill_attn.argtypes = [P, P, P, P, I, I, P, ctypes.c_size_t, P, P, P]
         lib.stv_lookup_workspace_bytes.restype = I
         lib.stv_lookup_workspace_bytes.argtypes = [I, P]
         lib.stv_lookup_draft.restype = I
@@ -338,3 +343,27 @@ def stv_lookup_draft(histories, min_len: int, max_len: int, k: int, n_prop, prop
         _ptr(prop, torch.int32, "prop"), _ptr(match_len, torch.int32, "match_len"),
         _ptr(match_pos, torch.int64, "match_pos"), _ptr(workspace, name="workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def stv_prefill_workspace_bytes(shape, seq, n_tokens: int) -> int:
+    arr = _seq_array([seq])
+    out = ctypes.c_size_t()
+    _check("stv_prefill_workspace_bytes", load().stv_prefill_workspace_bytes(
+        ctypes.byref(shape), arr, int(n_tokens), ctypes.byref(out)))
+    return out.value
+
+
+def stv_prefill_attn(shape, layer: LayerCache, seq, q, n_tokens: int, path, workspace, o, dev_status=None,
+                     stream=None):
+    """Prefill attention over the 3-bit cache (include/stv.h): q and o are
+    fp16 [n_tokens][hq][256]; the prompt's rows are already in the cache at
+    seq.ctx .. seq.ctx + n_tokens - 1."""
+    import torch
+
+    lc = layer.c()
+    arr = _seq_array([seq])
+    path = PATHS.get(path, path)
+    _check("stv_prefill_attn", load().stv_prefill_attn(
+        ctypes.byref(shape), ctypes.byref(lc), arr, _ptr(q, torch.float16, "q"), int(n_tokens), int(path),
+        _ptr(workspace, name="workspace"), workspace.numel() * workspace.element_size(),
+        _ptr(o, torch.float16, "o"), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))

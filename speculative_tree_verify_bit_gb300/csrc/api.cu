@@ -116,6 +116,53 @@ static int to_status(cudaError_t e) { return e == cudaSuccess ? STV_OK : STV_ERR
 
 using namespace stv;
 
+// Prefill launch planning (used by stv_prefill_* below).
+namespace {
+
+constexpr size_t kParentsBytes = ((size_t)STV_MAX_SEQS * kMaxT * sizeof(int32_t) + 255) / 256 * 256;
+
+int prefill_chunk_tokens(const stv_shape* sh) {
+  const int g = sh->hq / sh->hkv;
+  const int c = 128 / g;
+  return c < kMaxT ? c : kMaxT;
+}
+
+// The launches of a prefill: for each, the first prompt token, the chunk
+// size and the number of chunks.  Full chunks go STV_MAX_SEQS at a time; a
+// last partial chunk gets a launch of its own.
+struct PrefillLaunch {
+  int start, t, count;
+};
+
+template <typename F>
+int for_each_prefill_launch(int n_tokens, int c, F&& f) {
+  int start = 0;
+  while (start < n_tokens) {
+    const int full = (n_tokens - start) / c;
+    PrefillLaunch pl;
+    pl.start = start;
+    if (full > 0) {
+      pl.t = c;
+      pl.count = full < STV_MAX_SEQS ? full : STV_MAX_SEQS;
+    } else {
+      pl.t = n_tokens - start;
+      pl.count = 1;
+    }
+    if (int rc = f(pl)) return rc;
+    start += pl.t * pl.count;
+  }
+  return STV_OK;
+}
+
+void prefill_seqs(const stv_seq* seq, const PrefillLaunch& pl, stv_seq* out) {
+  for (int i = 0; i < pl.count; ++i) {
+    out[i] = *seq;
+    out[i].ctx = seq->ctx + pl.start + i * pl.t;
+  }
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* stv_status_string(int status) {
@@ -271,6 +318,61 @@ int stv_split_combine(const stv_shape* shape, const stv_seq* seqs, int n_seqs, i
   p.ml = reinterpret_cast<const float*>(ws + wl.off_ml);
   p.o = static_cast<__half*>(o);
   return to_status(launch_split_combine(p, (cudaStream_t)stream));
+}
+
+// ---------------------------------------------------------------------------
+// Prefill (next row f2): chunks of C prompt tokens as chain trees, up to
+// STV_MAX_SEQS chunks per verify launch, then the split merge.
+
+
+int stv_prefill_workspace_bytes(const stv_shape* shape, const stv_seq* seq, int n_tokens, size_t* bytes) {
+  if (!shape || !seq || !bytes || n_tokens < 1) return STV_ERR_INVALID_ARG;
+  ShapeInfo sh;
+  int rc = check_shape(shape, 1, &sh);
+  if (rc) return rc;
+  const int c = prefill_chunk_tokens(shape);
+  size_t most = 0;
+  rc = for_each_prefill_launch(n_tokens, c, [&](const PrefillLaunch& pl) -> int {
+    stv_seq seqs[STV_MAX_SEQS];
+    prefill_seqs(seq, pl, seqs);
+    size_t b = 0;
+    if (int r = stv_verify_workspace_bytes(shape, seqs, pl.count, pl.t, 0, &b)) return r;
+    most = b > most ? b : most;
+    return (int)STV_OK;
+  });
+  if (rc) return rc;
+  *bytes = kParentsBytes + most;
+  return STV_OK;
+}
+
+int stv_prefill_attn(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seq, const void* q,
+                     int n_tokens, int path, void* workspace, size_t ws_bytes, void* o, int32_t* dev_status,
+                     stv_stream_t stream) {
+  size_t need = 0;
+  int rc = stv_prefill_workspace_bytes(shape, seq, n_tokens, &need);
+  if (rc) return rc;
+  if (!layer || !q || !o || !workspace) return STV_ERR_INVALID_ARG;
+  if (ws_bytes < need) return STV_ERR_WORKSPACE_TOO_SMALL;
+  const int c = prefill_chunk_tokens(shape);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* parents = reinterpret_cast<int32_t*>(ws);
+  // chain parents for STV_MAX_SEQS chunks of c tokens; a last partial chunk
+  // of t < c tokens uses the first t entries, which are its chain too
+  if (cudaError_t e = launch_chain_parents(parents, STV_MAX_SEQS, c, (cudaStream_t)stream)) {
+    (void)e;
+    return STV_ERR_CUDA;
+  }
+  const size_t row = (size_t)shape->hq * kHeadDim;  // halves per token
+  return for_each_prefill_launch(n_tokens, c, [&](const PrefillLaunch& pl) -> int {
+    stv_seq seqs[STV_MAX_SEQS];
+    prefill_seqs(seq, pl, seqs);
+    const __half* qs = static_cast<const __half*>(q) + (size_t)pl.start * row;
+    __half* os = static_cast<__half*>(o) + (size_t)pl.start * row;
+    if (int r = verify_common(shape, layer, seqs, pl.count, nullptr, nullptr, qs, parents, pl.t, path,
+                              ws + kParentsBytes, ws_bytes - kParentsBytes, dev_status, stream))
+      return r;
+    return stv_split_combine(shape, seqs, pl.count, pl.t, ws + kParentsBytes, ws_bytes - kParentsBytes, os, stream);
+  });
 }
 
 int stv_tree_accept(const int32_t* parent, const int32_t* draft_ids, const int32_t* target_argmax, int t_nodes,

@@ -127,6 +127,7 @@ WsLayout ws_layout(const ShapeInfo& sh, int n_seqs, const Plan& plan);
 
 // ---- launchers (return cudaError_t of the launch) ----
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t s);
+cudaError_t launch_chain_parents(int32_t* parent, int chunks, int t, cudaStream_t s);
 cudaError_t launch_kv_commit(const CommitParams& p, cudaStream_t s);
 cudaError_t launch_quantize_q(const __half* q, int n_rows, int8_t* qi, float* sq, cudaStream_t s);
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);

@@ -163,4 +163,19 @@ cudaError_t launch_int8_dots(const VerifyParams& p, int seq, const __half* q_row
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Prefill (next row f2): chain trees, parent[c][i] = i - 1 for chunks of t
+// prompt tokens, whose ancestor-or-self masks are the causal mask.
+
+__global__ void __launch_bounds__(256) chain_parents_t_kernel(int32_t* parent, int chunks, int t) {
+  const int i = blockIdx.x * 256 + threadIdx.x;
+  if (i < chunks * t) parent[i] = (i % t) - 1;
+}
+
+cudaError_t launch_chain_parents(int32_t* parent, int chunks, int t, cudaStream_t s) {
+  const int n = chunks * t;
+  chain_parents_t_kernel<<<(n + 255) / 256, 256, 0, s>>>(parent, chunks, t);
+  return cudaGetLastError();
+}
+
 }  // namespace stv
