@@ -307,6 +307,55 @@ def measure_lookup(w: workloads.Workload, dev, reps: int = 50, min_len: int = 6,
             "proposed": int(n_prop.sum().item())}
 
 
+def measured_bf16_peak():
+    """Dense fp16/bf16 tensor peak (TFLOP/s, burst) from MEASURED_PEAKS.json."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def measure_prefill(dev, n: int = 32768, reps: int = 3, hq: int = 24, hkv: int = 4, path: str = "exact"):
+    """Prefill attention (stv_prefill_attn) of an n-token prompt on an empty
+    cache, one layer: the prompt's K/V are packed into the 3-bit cache, then
+    every token attends causally.  Algorithmic FLOPs = 4 hq D sum_t (t + 1)
+    (Q.K^T and P.V over the visible keys); tensor-bound in intent, so the
+    fraction is against the measured dense fp16/bf16 peak."""
+    import torch
+
+    import speculative_tree_verify_bit_gb300 as stv
+
+    pages = -(-n // 256) + 1
+    table = torch.as_tensor(np.random.default_rng(77).permutation(pages).astype(np.int32), device=dev)
+    k, v = workloads.kv_rows(4242, n, hkv, device=dev)
+    q = workloads.q_rows(4243, 1, n, hq, device=dev)[0].contiguous()
+    layer = stv.LayerCache.empty(pages, hkv, device=dev)
+    shape = stv.make_shape(hq, hkv)
+    stv.stv_kv_append_pack(shape, layer, [stv.Seq(table, 0)], k.contiguous(), v.contiguous(),
+                           torch.zeros(n, dtype=torch.int32, device=dev),
+                           torch.arange(n, dtype=torch.int32, device=dev))
+    seq = stv.Seq(table, 0)
+    ws = torch.empty(stv.stv_prefill_workspace_bytes(shape, seq, n), dtype=torch.uint8, device=dev)
+    o = torch.empty((n, hq, 256), dtype=torch.float16, device=dev)
+    stv.stv_prefill_attn(shape, layer, seq, q, n, path, ws, o)  # warm-up
+    times = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        stv.stv_prefill_attn(shape, layer, seq, q, n, path, ws, o)
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    flops = 4.0 * hq * 256 * (n * (n + 1) / 2)
+    peak, kind = measured_bf16_peak()
+    tflops = flops / (ms * 1e-3) / 1e12
+    return {"prompt_tokens": n, "layers": 1, "path": path, "ms_per_call": ms, "tokens_per_s": n / (ms * 1e-3),
+            "bound": "tensor", "tflops": tflops, "peak_tflops": peak, "frac": tflops / peak, "peak_source": kind}
+
+
 def max_over_ranks(values, dist=None, device="cpu"):
     """Each value's maximum over all ranks (the slowest replica sets the
     job's time); unchanged on one process."""
@@ -413,6 +462,7 @@ def run_gpu(args, rank, world):
 
     med_ms = statistics.median(round_ms)  # a round = one graph replay
     lookup = measure_lookup(w, dev) if rank == 0 else None
+    prefill = measure_prefill(dev) if rank == 0 else None
     med_ms, e2e_ms = max_over_ranks([med_ms, e2e_ms], dist, dev)
     layer_rounds = args.steps * r.L * world
     us_per_lr = us_per_layer_round(med_ms, r.L, world)
@@ -427,7 +477,7 @@ def run_gpu(args, rank, world):
                 peak=peak, peak_kind=peak_kind, achieved=achieved, clocks=clk.summary(), status=st, h2d=h2d,
                 d2h=d2h, launches=r.launches_per_step(args.path) * args.steps, p_accept=p_accept, traffic=traffic,
                 n_units=None, ws_bytes=r.ws_bytes, round_gbs=bytes_lr / (us_per_lr * 1e-6) / 1e9 / world,
-                lookup=lookup)
+                lookup=lookup, prefill=prefill)
 
 
 def load_traffic(workload, path):
@@ -584,7 +634,7 @@ def main():
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
         "dev_status": res["status"],
-        "next_rows": {"lookup_draft": res.get("lookup")},
+        "next_rows": {"lookup_draft": res.get("lookup"), "prefill_attn": res.get("prefill")},
     }
     print(json.dumps(line), flush=True)
 
