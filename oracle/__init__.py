@@ -34,6 +34,7 @@ HEAD_DIM = 256
 GROUP = 32
 PAGE_TOKENS = 256
 HEAD_BYTES = 57344
+HEAD_BYTES_I4 = 66560  # int4 per token and head (next row f3)
 
 
 def build(force: bool = False) -> str:
@@ -83,6 +84,8 @@ def _load():
             lib.orc_kv_commit.argtypes = [P, I64, I32, I32, P, P, P, I, P, P, I]
             lib.orc_decode_rows.restype = I
             lib.orc_decode_rows.argtypes = [P, I64, I32, I32, P, P, I, I64, I64, I, P]
+            lib.orc_quantize_row_i4.restype = None
+            lib.orc_quantize_row_i4.argtypes = [P, P, P]
             lib.orc_lookup_draft.restype = I
             lib.orc_lookup_draft.argtypes = [P, I64, I, I, I, P, P, P, P]
             _lib = lib
@@ -172,11 +175,14 @@ def check_tree(parent) -> bool:
 # --------------------------------------------------------------------------
 
 class Cache:
-    """A host-side paged 3-bit cache for one layer (bytes as uint8)."""
+    """A host-side paged cache for one layer (bytes as uint8): the 3-bit cache
+    (bits=3) or the int4 per-token-head cache (bits=4); the C side tells them
+    apart by the page stride."""
 
-    def __init__(self, hkv: int, pool_pages: int, pool: np.ndarray | None = None):
+    def __init__(self, hkv: int, pool_pages: int, pool: np.ndarray | None = None, bits: int = 3):
         self.hkv = int(hkv)
-        self.page_bytes = self.hkv * HEAD_BYTES
+        self.bits = int(bits)
+        self.page_bytes = self.hkv * (HEAD_BYTES if bits == 3 else HEAD_BYTES_I4)
         self.pool_pages = int(pool_pages)
         if pool is None:
             pool = np.zeros(self.page_bytes * self.pool_pages, np.uint8)
@@ -304,3 +310,14 @@ def lookup_draft(history, min_len: int = 6, max_len: int = 12, k: int = 15):
     if rc != 0:
         raise ValueError("orc_lookup_draft: bad lengths")
     return prop[:n_prop.value].copy(), mlen.value, mpos.value
+
+
+def quantize_row_i4(x):
+    """int4 per-token-head quantizer (stv_oracle.c, orc_quantize_row_i4):
+    256 fp16 values -> (fp16 scale bits, codes u = c + 8 in 0..15)."""
+    xh = np.ascontiguousarray(np.asarray(x, np.float16).view(np.uint16))
+    assert xh.size == HEAD_DIM
+    s = np.zeros(1, np.uint16)
+    u = np.zeros(HEAD_DIM, np.uint8)
+    _load().orc_quantize_row_i4(_p(xh), _p(s), _p(u))
+    return s[0], u

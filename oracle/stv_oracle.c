@@ -79,6 +79,8 @@ enum {
 
 int orc_head_bytes(void) { return HEAD_BYTES; }
 
+
+
 /* ------------------------------------------------------------------------ */
 /* IEEE binary16 <-> binary64.                                              */
 /* ------------------------------------------------------------------------ */
@@ -119,6 +121,49 @@ uint16_t orc_double_to_half(double x) {
 }
 
 float orc_double_to_float(double x) { return (float)x; }
+
+/* ------------------------------------------------------------------------
+ * Second cache format (next row f3): int4 with one scale per token and KV
+ * head ("elpis" README mirror, syv-ai README, int4 KV section: the stock
+ * int4_per_token_head cache).  Reading (the pages give no formula): per
+ * (token, KV head) m = max|x| over its 256 values, s = fp16(m / 7),
+ * c = clamp(rne(x / s), -8, 7) (all 0 when s == 0), stored as u = c + 8 in 4
+ * bits; decoded value s * c.  Layout per KV head (66,560 bytes): K codes
+ * [256 tok][32 words], K scales [256] fp16, V codes [4 tiles of 64 tok]
+ * [256 ch][8 words] (channel-major: a word holds one channel's codes for 8
+ * tokens), V scales [256] fp16.  Inside a word of 8 elements e0..e7,
+ * element e sits at bit 4*(e/2) (even e) or 16 + 4*(e/2) (odd e).
+ * The format of a pool follows from its page stride: hkv * 57,344 bytes for
+ * the 3-bit cache, hkv * 66,560 for this one.
+ */
+#define I4_OFF_K_CODES 0
+#define I4_OFF_K_SCALES (PAGE_TOK * 128)                /* 32768 */
+#define I4_OFF_V_CODES (I4_OFF_K_SCALES + PAGE_TOK * 2)  /* 33280 */
+#define I4_OFF_V_SCALES (I4_OFF_V_CODES + PAGE_TOK * 128) /* 66048 */
+#define I4_HEAD_BYTES (I4_OFF_V_SCALES + PAGE_TOK * 2)   /* 66560 */
+
+int orc_head_bytes_i4(void) { return I4_HEAD_BYTES; }
+
+/* Bit position of element e (0..7) inside its word. */
+static int i4_pos(int e) { return ((e & 1) ? 16 : 0) + 4 * (e >> 1); }
+
+/* Quantize one token-head row of 256 fp16 values: scale and codes u = c + 8. */
+void orc_quantize_row_i4(const uint16_t* x, uint16_t* s_out, uint8_t* u) {
+  double m = 0.0;
+  for (int i = 0; i < HEAD_DIM; ++i) {
+    double a = fabs(orc_half_to_double(x[i]));
+    if (a > m) m = a;
+  }
+  uint16_t s = orc_double_to_half(m / 7.0);
+  double sd = orc_half_to_double(s);
+  for (int i = 0; i < HEAD_DIM; ++i) {
+    double c = sd == 0.0 ? 0.0 : rint(orc_half_to_double(x[i]) / sd);
+    if (c < -8.0) c = -8.0;
+    if (c > 7.0) c = 7.0;
+    u[i] = (uint8_t)(c + 8.0);
+  }
+  *s_out = s;
+}
 
 /* ------------------------------------------------------------------------ */
 /* 3-bit group quantizer and the block bit layout.                          */
@@ -199,7 +244,23 @@ typedef struct {
   int32_t hkv;
   const int32_t* page_tables; /* all sequences' tables, concatenated */
   const int32_t* pt_offsets;  /* [n_seqs + 1] */
+  int fmt;                    /* 0: 3-bit groups of 32, 1: int4 per token and head */
+  int64_t head_bytes;
 } cache_view;
+
+/* The pool's format from its page stride; ORC_BAD_ARG if it is neither. */
+static int view_format(cache_view* cv) {
+  if (cv->page_bytes == (int64_t)cv->hkv * HEAD_BYTES) {
+    cv->fmt = 0;
+    cv->head_bytes = HEAD_BYTES;
+  } else if (cv->page_bytes == (int64_t)cv->hkv * I4_HEAD_BYTES) {
+    cv->fmt = 1;
+    cv->head_bytes = I4_HEAD_BYTES;
+  } else {
+    return ORC_BAD_ARG;
+  }
+  return ORC_OK;
+}
 
 /* Base of KV head h's block for token `tok` of sequence `seq`, or NULL. */
 static uint8_t* head_block(const cache_view* cv, int seq, int64_t tok, int h) {
@@ -208,7 +269,7 @@ static uint8_t* head_block(const cache_view* cv, int seq, int64_t tok, int h) {
   if (tok < 0 || lp >= np) return NULL;
   int32_t page = cv->page_tables[cv->pt_offsets[seq] + lp];
   if (page < 0 || page >= cv->pool_pages) return NULL;
-  return cv->pool + (int64_t)page * cv->page_bytes + (int64_t)h * HEAD_BYTES;
+  return cv->pool + (int64_t)page * cv->page_bytes + (int64_t)h * cv->head_bytes;
 }
 
 static void load_words(const uint8_t* p, uint32_t* w) { memcpy(w, p, 12); }
@@ -233,10 +294,30 @@ static uint8_t* v_scale(uint8_t* hb, int slot, int g) {
 }
 
 /* Decode K (which = 0) or V (which = 1) of one token and head: 256 values. */
+/* int4 cache: code u of element `ch` (K) or `slot` (V) of one token and head. */
+static int i4_code(uint8_t* hb, int which, int slot, int ch) {
+  uint32_t w;
+  if (which == 0) {
+    memcpy(&w, hb + I4_OFF_K_CODES + slot * 128 + (ch / 8) * 4, 4);
+    return (int)((w >> i4_pos(ch % 8)) & 15u);
+  }
+  int within = slot % TILE_TOK;
+  memcpy(&w, hb + I4_OFF_V_CODES + (slot / TILE_TOK) * (HEAD_DIM * 32) + ch * 32 + (within / 8) * 4, 4);
+  return (int)((w >> i4_pos(within % 8)) & 15u);
+}
+static uint8_t* i4_scale(uint8_t* hb, int which, int slot) {
+  return hb + (which == 0 ? I4_OFF_K_SCALES : I4_OFF_V_SCALES) + slot * 2;
+}
+
 static int decode_row(const cache_view* cv, int seq, int64_t tok, int h, int which, double* out) {
   uint8_t* hb = head_block(cv, seq, tok, h);
   if (!hb) return ORC_BAD_PAGE;
   int slot = (int)(tok % PAGE_TOK);
+  if (cv->fmt == 1) {
+    double s = orc_half_to_double(load_u16(i4_scale(hb, which, slot)));
+    for (int c = 0; c < HEAD_DIM; ++c) out[c] = s * (i4_code(hb, which, slot, c) - 8);
+    return ORC_OK;
+  }
   for (int g = 0; g < N_GROUPS; ++g) {
     if (which == 0) {
       uint32_t w[3];
@@ -255,16 +336,24 @@ static int decode_row(const cache_view* cv, int seq, int64_t tok, int h, int whi
   return ORC_OK;
 }
 
-/* K codes (0..7) and scales of one token and head, for the int8 definition. */
-static int k_codes_row(const cache_view* cv, int seq, int64_t tok, int h, uint8_t* codes, double* scales) {
+/* K's integer values (code - 4 for the 3-bit cache, u - 8 for int4) and
+ * per-group scales of one token and head, for the int8 definition (the
+ * int4 cache has one scale per token: every group gets it). */
+static int k_codes_row(const cache_view* cv, int seq, int64_t tok, int h, int8_t* kv, double* scales) {
   uint8_t* hb = head_block(cv, seq, tok, h);
   if (!hb) return ORC_BAD_PAGE;
   int slot = (int)(tok % PAGE_TOK);
+  if (cv->fmt == 1) {
+    double s = orc_half_to_double(load_u16(i4_scale(hb, 0, slot)));
+    for (int g = 0; g < N_GROUPS; ++g) scales[g] = s;
+    for (int c = 0; c < HEAD_DIM; ++c) kv[c] = (int8_t)(i4_code(hb, 0, slot, c) - 8);
+    return ORC_OK;
+  }
   for (int g = 0; g < N_GROUPS; ++g) {
     uint32_t w[3];
     load_words(k_words(hb, slot, g), w);
     scales[g] = orc_half_to_double(load_u16(k_scale(hb, slot, g)));
-    for (int i = 0; i < GROUP; ++i) codes[g * GROUP + i] = orc_block_code(w, i);
+    for (int i = 0; i < GROUP; ++i) kv[g * GROUP + i] = (int8_t)((int)orc_block_code(w, i) - 4);
   }
   return ORC_OK;
 }
@@ -278,6 +367,7 @@ int orc_kv_append(uint8_t* pool, int64_t page_bytes, int32_t pool_pages, int32_t
                   const uint16_t* k, const uint16_t* v, /* [n_rows][hkv][256] */
                   const int32_t* row_seq, const int32_t* row_pos, int n_rows) {
   cache_view cv = {pool, page_bytes, pool_pages, hkv, page_tables, pt_offsets};
+  if (view_format(&cv) != ORC_OK) return ORC_BAD_ARG;
   for (int r = 0; r < n_rows; ++r) {
     int seq = row_seq[r];
     if (seq < 0 || seq >= n_seqs) return ORC_BAD_ARG;
@@ -287,6 +377,28 @@ int orc_kv_append(uint8_t* pool, int64_t page_bytes, int32_t pool_pages, int32_t
       int slot = row_pos[r] % PAGE_TOK;
       const uint16_t* kr = k + ((int64_t)r * hkv + h) * HEAD_DIM;
       const uint16_t* vr = v + ((int64_t)r * hkv + h) * HEAD_DIM;
+      if (cv.fmt == 1) { /* int4 per token and head */
+        uint16_t s;
+        uint8_t u[HEAD_DIM];
+        orc_quantize_row_i4(kr, &s, u);
+        for (int wd = 0; wd < HEAD_DIM / 8; ++wd) {
+          uint32_t w = 0;
+          for (int e = 0; e < 8; ++e) w |= (uint32_t)u[8 * wd + e] << i4_pos(e);
+          memcpy(hb + I4_OFF_K_CODES + slot * 128 + wd * 4, &w, 4);
+        }
+        store_u16(i4_scale(hb, 0, slot), s);
+        orc_quantize_row_i4(vr, &s, u);
+        store_u16(i4_scale(hb, 1, slot), s);
+        int within = slot % TILE_TOK;
+        for (int c = 0; c < HEAD_DIM; ++c) {
+          uint8_t* p = hb + I4_OFF_V_CODES + (slot / TILE_TOK) * (HEAD_DIM * 32) + c * 32 + (within / 8) * 4;
+          uint32_t w;
+          memcpy(&w, p, 4);
+          w = (w & ~(15u << i4_pos(within % 8))) | ((uint32_t)u[c] << i4_pos(within % 8));
+          memcpy(p, &w, 4);
+        }
+        continue;
+      }
       for (int g = 0; g < N_GROUPS; ++g) {
         uint16_t s;
         uint8_t codes[GROUP];
@@ -352,10 +464,10 @@ void orc_quantize_q_int8(const uint16_t* q, int8_t* qi, float* sq) {
 }
 
 /* Integer per-group dots I_g = sum_{c in g} qi_c * (code_c - 4). */
-static void int8_group_dots(const int8_t* qi, const uint8_t* codes, int64_t* dots) {
+static void int8_group_dots(const int8_t* qi, const int8_t* kv, int64_t* dots) {
   for (int g = 0; g < N_GROUPS; ++g) {
     int64_t acc = 0;
-    for (int i = 0; i < GROUP; ++i) acc += (int64_t)qi[g * GROUP + i] * ((int)codes[g * GROUP + i] - 4);
+    for (int i = 0; i < GROUP; ++i) acc += (int64_t)qi[g * GROUP + i] * (int64_t)kv[g * GROUP + i];
     dots[g] = acc;
   }
 }
@@ -421,11 +533,11 @@ static int attention_row(attn_job* jb, int r) {
       for (int c = 0; c < HEAD_DIM; ++c) s += qd[c] * kd[c];
       s /= 16.0;
     } else {
-      uint8_t codes[HEAD_DIM];
+      int8_t kv[HEAD_DIM];
       double sk[N_GROUPS];
       int64_t dots[N_GROUPS];
-      rc = k_codes_row(cv, seq, keys[a], h, codes, sk);
-      int8_group_dots(qi, codes, dots);
+      rc = k_codes_row(cv, seq, keys[a], h, kv, sk);
+      int8_group_dots(qi, kv, dots);
       for (int g = 0; g < N_GROUPS; ++g) s += sk[g] * (double)dots[g];
       s = (double)sq * s / 16.0;
     }
@@ -479,6 +591,7 @@ int orc_attention(const uint8_t* pool, int64_t page_bytes, int32_t pool_pages, i
   for (int r = 0; r < n_rows; ++r)
     if (rows[3 * r] < 0 || rows[3 * r] >= n_seqs) return ORC_BAD_ARG;
   cache_view cv = {(uint8_t*)pool, page_bytes, pool_pages, hkv, page_tables, pt_offsets};
+  if (view_format(&cv) != ORC_OK) return ORC_BAD_ARG;
   attn_job jb;
   jb.cv = &cv;
   jb.ctx = ctx;
@@ -512,16 +625,17 @@ int orc_int8_dots(const uint8_t* pool, int64_t page_bytes, int32_t pool_pages, i
                   const int32_t* page_tables, const int32_t* pt_offsets, int seq, const uint16_t* qrow,
                   int qhead, int64_t tok_begin, int64_t tok_end, int32_t* out) {
   cache_view cv = {(uint8_t*)pool, page_bytes, pool_pages, hkv, page_tables, pt_offsets};
+  if (view_format(&cv) != ORC_OK) return ORC_BAD_ARG;
   int h = qhead / (hq / hkv);
   int8_t qi[HEAD_DIM];
   float sq;
   orc_quantize_q_int8(qrow, qi, &sq);
   for (int64_t j = tok_begin; j < tok_end; ++j) {
-    uint8_t codes[HEAD_DIM];
+    int8_t kv[HEAD_DIM];
     double sk[N_GROUPS];
     int64_t dots[N_GROUPS];
-    if (k_codes_row(&cv, seq, j, h, codes, sk) != ORC_OK) return ORC_BAD_PAGE;
-    int8_group_dots(qi, codes, dots);
+    if (k_codes_row(&cv, seq, j, h, kv, sk) != ORC_OK) return ORC_BAD_PAGE;
+    int8_group_dots(qi, kv, dots);
     for (int g = 0; g < N_GROUPS; ++g) out[(j - tok_begin) * N_GROUPS + g] = (int32_t)dots[g];
   }
   return ORC_OK;
@@ -588,10 +702,41 @@ int orc_kv_commit(uint8_t* pool, int64_t page_bytes, int32_t pool_pages, int32_t
                   const int32_t* pt_offsets, const int32_t* ctx, int n_seqs, const int32_t* n_commit,
                   const int32_t* path, int t) {
   cache_view cv = {pool, page_bytes, pool_pages, hkv, page_tables, pt_offsets};
+  if (view_format(&cv) != ORC_OK) return ORC_BAD_ARG;
   for (int s = 0; s < n_seqs; ++s) {
     int n = n_commit[s];
     if (n < 1 || n > t) return ORC_BAD_ARG;
     for (int h = 0; h < hkv; ++h) {
+      if (cv.fmt == 1) { /* int4: K codes and both scales move whole; V nibbles channel by channel */
+        uint8_t kc4[32][128], sc4[32][4], vu[32][HEAD_DIM];
+        for (int i = 0; i < n; ++i) {
+          int64_t src = (int64_t)ctx[s] + path[(int64_t)s * t + i];
+          uint8_t* hb = head_block(&cv, s, src, h);
+          if (!hb) return ORC_BAD_PAGE;
+          int slot = (int)(src % PAGE_TOK);
+          memcpy(kc4[i], hb + I4_OFF_K_CODES + slot * 128, 128);
+          memcpy(sc4[i], i4_scale(hb, 0, slot), 2);
+          memcpy(sc4[i] + 2, i4_scale(hb, 1, slot), 2);
+          for (int c = 0; c < HEAD_DIM; ++c) vu[i][c] = (uint8_t)i4_code(hb, 1, slot, c);
+        }
+        for (int i = 0; i < n; ++i) {
+          int64_t dst = (int64_t)ctx[s] + i;
+          uint8_t* hb = head_block(&cv, s, dst, h);
+          if (!hb) return ORC_BAD_PAGE;
+          int slot = (int)(dst % PAGE_TOK), within = slot % TILE_TOK;
+          memcpy(hb + I4_OFF_K_CODES + slot * 128, kc4[i], 128);
+          memcpy(i4_scale(hb, 0, slot), sc4[i], 2);
+          memcpy(i4_scale(hb, 1, slot), sc4[i] + 2, 2);
+          for (int c = 0; c < HEAD_DIM; ++c) {
+            uint8_t* p = hb + I4_OFF_V_CODES + (slot / TILE_TOK) * (HEAD_DIM * 32) + c * 32 + (within / 8) * 4;
+            uint32_t w;
+            memcpy(&w, p, 4);
+            w = (w & ~(15u << i4_pos(within % 8))) | ((uint32_t)vu[i][c] << i4_pos(within % 8));
+            memcpy(p, &w, 4);
+          }
+        }
+        continue;
+      }
       /* Copy every source row out first, then write: a destination slot may
        * be the source slot of a later row. */
       uint8_t kc[32][96], ks[32][16], vs[32][16], vc[32][HEAD_DIM];
@@ -635,6 +780,7 @@ int orc_decode_rows(const uint8_t* pool, int64_t page_bytes, int32_t pool_pages,
                     const int32_t* page_tables, const int32_t* pt_offsets, int seq, int64_t tok_begin,
                     int64_t tok_end, int which, double* out /* [n_tok][hkv][256] */) {
   cache_view cv = {(uint8_t*)pool, page_bytes, pool_pages, hkv, page_tables, pt_offsets};
+  if (view_format(&cv) != ORC_OK) return ORC_BAD_ARG;
   for (int64_t j = tok_begin; j < tok_end; ++j)
     for (int h = 0; h < hkv; ++h) {
       int rc = decode_row(&cv, seq, j, h, which, out + ((j - tok_begin) * hkv + h) * HEAD_DIM);
