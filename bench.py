@@ -181,7 +181,7 @@ class GpuRound:
     """All layers of one workload resident on the GPU, plus one round's inputs."""
 
     def __init__(self, w: workloads.Workload, p_accept: float, device, layers: int | None = None,
-                 fuse_append: bool = False):
+                 fuse_append: bool = False, group: int = 32):
         import torch
 
         import speculative_tree_verify_bit_gb300 as stv
@@ -190,7 +190,7 @@ class GpuRound:
         self.fuse_append = fuse_append
         self.L = layers or w.layers
         self.T, self.hq, self.hkv = w.t_nodes, w.hq, w.hkv
-        self.shape = stv.make_shape(self.hq, self.hkv)
+        self.shape = stv.make_shape(self.hq, self.hkv, group)
         self.pool_pages, tables = workloads.page_tables_for(w)
         self.tables = tables
         self.seqs = [stv.Seq(torch.as_tensor(t, device=device), c) for t, c in zip(tables, w.ctx)]
@@ -207,7 +207,7 @@ class GpuRound:
         self.row_pos = torch.cat([torch.arange(c, c + T, dtype=torch.int32, device=device) for c in w.ctx])
         for l in range(self.L):
             seed = workloads.layer_seed(w, l)
-            layer = stv.LayerCache.empty(self.pool_pages, self.hkv, device=device)
+            layer = stv.LayerCache.empty(self.pool_pages, self.hkv, device=device, group=group)
             ks, vs, kt, vt = [], [], [], []
             for s, c in enumerate(w.ctx):
                 k, v = workloads.kv_rows(seed + 7919 * s, c + T, self.hkv, device=device)
@@ -356,6 +356,48 @@ def measure_prefill(dev, n: int = 32768, reps: int = 3, hq: int = 24, hkv: int =
             "bound": "tensor", "tflops": tflops, "peak_tflops": peak, "frac": tflops / peak, "peak_source": kind}
 
 
+def int4_verify_bytes(ctx_list, t, hq=24, hkv=4):
+    """Bytes one verify launch must read from the int4 per-token-head cache:
+    128 B of K codes + 2 B of K scale and the same for V per token and KV
+    head, for every visible key, and Q."""
+    return sum(c + t for c in ctx_list) * hkv * 2 * (128 + 2) + len(ctx_list) * t * hq * 256 * 2
+
+
+def measure_int4(w: workloads.Workload, p_accept: float, dev, path: str = "exact", reps: int = 10):
+    """The same round over the int4 per-token-head cache (group 256): two
+    layers resident, eager rounds with events around each verify launch; the
+    layers alternate, so a launch does not find its cache in L2 (one layer's
+    cache is larger than L2 at 262K)."""
+    import torch
+
+    r = GpuRound(w, p_accept, dev, layers=2, group=256)
+    for _ in range(3):
+        r.step(path)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(r.L)]
+    times, rounds = [], []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        r.step(path, verify_events=ev)
+        b.record()
+        torch.cuda.synchronize()
+        times += [x.elapsed_time(y) for x, y in ev]
+        rounds.append(a.elapsed_time(b))
+    st = int(r.status.item())
+    v_us = statistics.median(times) * 1e3
+    vbytes = int4_verify_bytes(w.ctx, w.t_nodes, w.hq, w.hkv)
+    peak, kind = measured_peak()
+    gbs = vbytes / (v_us * 1e-6) / 1e9
+    out = {"workload": w.name, "group": 256, "path": path, "verify_us_per_launch": v_us,
+           "eager_us_per_layer_round": statistics.median(rounds) * 1e3 / r.L, "bound": "hbm",
+           "algorithmic_bytes_per_launch": vbytes, "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak,
+           "peak_source": kind, "dev_status": st}
+    del r
+    torch.cuda.empty_cache()
+    return out
+
+
 def max_over_ranks(values, dist=None, device="cpu"):
     """Each value's maximum over all ranks (the slowest replica sets the
     job's time); unchanged on one process."""
@@ -463,6 +505,7 @@ def run_gpu(args, rank, world):
     med_ms = statistics.median(round_ms)  # a round = one graph replay
     lookup = measure_lookup(w, dev) if rank == 0 else None
     prefill = measure_prefill(dev) if rank == 0 else None
+    int4 = measure_int4(w, p_accept, dev, args.path) if rank == 0 else None
     med_ms, e2e_ms = max_over_ranks([med_ms, e2e_ms], dist, dev)
     layer_rounds = args.steps * r.L * world
     us_per_lr = us_per_layer_round(med_ms, r.L, world)
@@ -477,7 +520,7 @@ def run_gpu(args, rank, world):
                 peak=peak, peak_kind=peak_kind, achieved=achieved, clocks=clk.summary(), status=st, h2d=h2d,
                 d2h=d2h, launches=r.launches_per_step(args.path) * args.steps, p_accept=p_accept, traffic=traffic,
                 n_units=None, ws_bytes=r.ws_bytes, round_gbs=bytes_lr / (us_per_lr * 1e-6) / 1e9 / world,
-                lookup=lookup, prefill=prefill)
+                lookup=lookup, prefill=prefill, int4=int4)
 
 
 def load_traffic(workload, path):
@@ -634,7 +677,8 @@ def main():
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
         "dev_status": res["status"],
-        "next_rows": {"lookup_draft": res.get("lookup"), "prefill_attn": res.get("prefill")},
+        "next_rows": {"lookup_draft": res.get("lookup"), "prefill_attn": res.get("prefill"),
+                      "int4_cache_verify": res.get("int4")},
     }
     print(json.dumps(line), flush=True)
 

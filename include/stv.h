@@ -69,6 +69,8 @@ typedef struct CUstream_st* stv_stream_t;
 #define STV_GROUP 32
 #define STV_PAGE_TOKENS 256
 #define STV_HEAD_BLOCK_BYTES 57344
+#define STV_GROUP_INT4 256            /* group of the int4 per-token-head cache */
+#define STV_HEAD_BLOCK_BYTES_INT4 66560
 
 enum stv_status {
   STV_OK = 0,
@@ -94,13 +96,19 @@ typedef struct {
   int32_t hq;          /* query heads (24 for the pages' model) */
   int32_t hkv;         /* KV heads (4) */
   int32_t head_dim;    /* must be 256 */
-  int32_t group;       /* quantization group, must be 32 */
+  int32_t group;       /* cache format, by its quantization group:
+                        *   32  (STV_GROUP): 3-bit codes, one fp16 scale per
+                        *       32 channels -- the pages' cache;
+                        *   256 (STV_GROUP_INT4): int4 codes, one fp16 scale
+                        *       per token and KV head (next row f3; see the
+                        *       int4 notes below) */
   int32_t page_tokens; /* must be 256 */
 } stv_shape;
 
 typedef struct {
   uint8_t* pool;      /* device: n_pages * page_bytes bytes */
-  int64_t page_bytes; /* must equal hkv * STV_HEAD_BLOCK_BYTES */
+  int64_t page_bytes; /* must equal hkv * STV_HEAD_BLOCK_BYTES (group 32) or
+                       * hkv * STV_HEAD_BLOCK_BYTES_INT4 (group 256) */
   int32_t n_pages;
 } stv_layer_cache;
 
@@ -116,7 +124,20 @@ const char* stv_status_string(int status);
 /* Library ABI version (monotonic). */
 int stv_version(void);
 
-/* Bytes of one page for `shape` (hkv * 57,344). */
+/* Bytes of one page for `shape` (hkv * 57,344; hkv * 66,560 for group 256).
+ *
+ * The int4 per-token-head cache (group 256; syv-ai README (mirror), int4 KV
+ * section: the stock int4_per_token_head cache; the pages give no formula).
+ * Reading: per (token, KV head) s = fp16(max|x| / 7), c = clamp(rne(x / s),
+ * -8, 7) (all 0 when s == 0), stored as u = c + 8; decoded value s * c.
+ * Per KV head (66,560 bytes): K codes [256 tok][32 words] at 0, K scales
+ * [256] fp16 at 32,768, V codes [4 tiles of 64 tok][256 ch][8 words] at
+ * 33,280 (a word holds one channel's codes for 8 tokens), V scales [256]
+ * fp16 at 66,048.  In a word of 8 elements e0..e7, element e sits at bit
+ * 4 * (e / 2), plus 16 when e is odd.  stv_kv_append_pack, stv_verify_attn,
+ * stv_split_combine, stv_verify_attn_no_alloc, stv_prefill_attn and
+ * stv_kv_commit accept it; stv_append_verify_attn and stv_int8_qk_dots return
+ * STV_ERR_UNIMPLEMENTED for it. */
 int stv_page_bytes(const stv_shape* shape, int64_t* bytes);
 
 /*

@@ -37,6 +37,8 @@ HEAD_DIM = 256
 GROUP = 32
 PAGE_TOKENS = 256
 HEAD_BLOCK_BYTES = 57344
+GROUP_INT4 = 256                # the int4 per-token-head cache (include/stv.h)
+HEAD_BLOCK_BYTES_INT4 = 66560
 
 # Every symbol include/stv.h declares.
 EXPORTS = (
@@ -152,27 +154,34 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def make_shape(hq: int = 24, hkv: int = 4) -> stv_shape:
-    return stv_shape(hq, hkv, HEAD_DIM, GROUP, PAGE_TOKENS)
+def make_shape(hq: int = 24, hkv: int = 4, group: int = GROUP) -> stv_shape:
+    """group 32: the 3-bit cache; group 256 (GROUP_INT4): the int4
+    per-token-head cache."""
+    return stv_shape(hq, hkv, HEAD_DIM, group, PAGE_TOKENS)
+
+
+def head_block_bytes(group: int = GROUP) -> int:
+    return HEAD_BLOCK_BYTES_INT4 if group == GROUP_INT4 else HEAD_BLOCK_BYTES
 
 
 class LayerCache:
     """One layer's paged pool: a uint8 CUDA tensor of n_pages * page_bytes."""
 
-    def __init__(self, pool, hkv: int):
+    def __init__(self, pool, hkv: int, group: int = GROUP):
         import torch
 
         self.hkv = hkv
-        self.page_bytes = hkv * HEAD_BLOCK_BYTES
+        self.group = group
+        self.page_bytes = hkv * head_block_bytes(group)
         assert pool.dtype == torch.uint8 and pool.numel() % self.page_bytes == 0
         self.pool = pool
         self.n_pages = pool.numel() // self.page_bytes
 
     @classmethod
-    def empty(cls, n_pages: int, hkv: int = 4, device="cuda"):
+    def empty(cls, n_pages: int, hkv: int = 4, device="cuda", group: int = GROUP):
         import torch
 
-        return cls(torch.zeros(n_pages * hkv * HEAD_BLOCK_BYTES, dtype=torch.uint8, device=device), hkv)
+        return cls(torch.zeros(n_pages * hkv * head_block_bytes(group), dtype=torch.uint8, device=device), hkv, group)
 
     def c(self) -> stv_layer_cache:
         return stv_layer_cache(_ptr(self.pool, name="pool").value, self.page_bytes, self.n_pages)

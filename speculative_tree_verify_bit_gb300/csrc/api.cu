@@ -11,7 +11,8 @@ namespace stv {
 
 static int check_shape(const stv_shape* sh, int t_nodes, ShapeInfo* out) {
   if (!sh) return STV_ERR_INVALID_ARG;
-  if (sh->head_dim != kHeadDim || sh->group != kGroup || sh->page_tokens != kPageTok) return STV_ERR_SHAPE_UNSUPPORTED;
+  if (sh->head_dim != kHeadDim || sh->page_tokens != kPageTok) return STV_ERR_SHAPE_UNSUPPORTED;
+  if (sh->group != kGroup && sh->group != kGroupI4) return STV_ERR_SHAPE_UNSUPPORTED;
   if (sh->hkv < 1 || sh->hq < sh->hkv || sh->hq % sh->hkv != 0) return STV_ERR_SHAPE_UNSUPPORTED;
   const int G = sh->hq / sh->hkv;
   if (t_nodes >= 0) {
@@ -24,13 +25,14 @@ static int check_shape(const stv_shape* sh, int t_nodes, ShapeInfo* out) {
     out->G = G;
     out->T = t_nodes;
     out->R = t_nodes * G;
+    out->i4 = sh->group == kGroupI4;
   }
   return STV_OK;
 }
 
-static int check_layer(const stv_layer_cache* l, int hkv) {
+static int check_layer(const stv_layer_cache* l, const ShapeInfo& sh) {
   if (!l || !l->pool || l->n_pages < 1) return STV_ERR_INVALID_ARG;
-  if (l->page_bytes != (int64_t)hkv * kHeadBytes) return STV_ERR_SHAPE_UNSUPPORTED;
+  if (l->page_bytes != (int64_t)sh.hkv * (sh.i4 ? kI4HeadBytes : kHeadBytes)) return STV_ERR_SHAPE_UNSUPPORTED;
   return STV_OK;
 }
 
@@ -183,7 +185,7 @@ int stv_page_bytes(const stv_shape* shape, int64_t* bytes) {
   int rc = check_shape(shape, -1, nullptr);
   if (rc) return rc;
   if (!bytes) return STV_ERR_INVALID_ARG;
-  *bytes = (int64_t)shape->hkv * kHeadBytes;
+  *bytes = (int64_t)shape->hkv * (shape->group == kGroupI4 ? kI4HeadBytes : kHeadBytes);
   return STV_OK;
 }
 
@@ -193,7 +195,7 @@ int stv_kv_append_pack(const stv_shape* shape, const stv_layer_cache* layer, con
   ShapeInfo sh;
   int rc = check_shape(shape, -1, &sh);
   if (rc) return rc;
-  if ((rc = check_layer(layer, sh.hkv)) || (rc = check_seqs(seqs, n_seqs, -1))) return rc;
+  if ((rc = check_layer(layer, sh)) || (rc = check_seqs(seqs, n_seqs, -1))) return rc;
   if (n_rows < 0 || (n_rows > 0 && (!k || !v || !row_seq || !row_pos))) return STV_ERR_INVALID_ARG;
   if (n_rows == 0) return STV_OK;
   AppendParams p;
@@ -209,6 +211,7 @@ int stv_kv_append_pack(const stv_shape* shape, const stv_layer_cache* layer, con
   p.row_seq = row_seq;
   p.row_pos = row_pos;
   p.n_rows = n_rows;
+  p.i4 = sh.i4;
   p.status = dev_status;
   return to_status(launch_kv_append(p, (cudaStream_t)stream));
 }
@@ -234,8 +237,9 @@ static int verify_common(const stv_shape* shape, const stv_layer_cache* layer, c
   ShapeInfo sh;
   int rc = check_shape(shape, t_nodes, &sh);
   if (rc) return rc;
-  if ((rc = check_layer(layer, sh.hkv)) || (rc = check_seqs(seqs, n_seqs, t_nodes))) return rc;
+  if ((rc = check_layer(layer, sh)) || (rc = check_seqs(seqs, n_seqs, t_nodes))) return rc;
   if (!q || !parent || !workspace || (path != STV_PATH_EXACT && path != STV_PATH_INT8)) return STV_ERR_INVALID_ARG;
+  if (k_tree && sh.i4) return STV_ERR_UNIMPLEMENTED;  // the fused append packs the 3-bit cache only
   int sm = 0;
   if ((rc = device_sm_count(&sm))) return rc;
   Plan plan;
@@ -266,6 +270,7 @@ static int verify_common(const stv_shape* shape, const stv_layer_cache* layer, c
   p.ml = reinterpret_cast<float*>(ws + wl.off_ml);
   p.k_tree = static_cast<const __half*>(k_tree);
   p.v_tree = static_cast<const __half*>(v_tree);
+  p.i4 = sh.i4;
   p.status = dev_status;
   cudaStream_t s = (cudaStream_t)stream;
   if (path == STV_PATH_INT8) {
@@ -396,7 +401,7 @@ int stv_kv_commit(const stv_shape* shape, const stv_layer_cache* layers, int n_l
   CommitParams p;
   memset(&p, 0, sizeof(p));
   for (int l = 0; l < n_layers; ++l) {
-    if ((rc = check_layer(&layers[l], sh.hkv))) return rc;
+    if ((rc = check_layer(&layers[l], sh))) return rc;
     p.pools[l] = layers[l].pool;
     p.pool_pages[l] = layers[l].n_pages;
   }
@@ -409,6 +414,7 @@ int stv_kv_commit(const stv_shape* shape, const stv_layer_cache* layers, int n_l
   p.n_commit = n_commit;
   p.path = path;
   p.ctx_dev = ctx_dev;
+  p.i4 = sh.i4;
   p.status = dev_status;
   return to_status(launch_kv_commit(p, (cudaStream_t)stream));
 }
@@ -419,7 +425,8 @@ int stv_int8_qk_dots(const stv_shape* shape, const stv_layer_cache* layer, const
   ShapeInfo sh;
   int rc = check_shape(shape, -1, &sh);
   if (rc) return rc;
-  if ((rc = check_layer(layer, sh.hkv)) || (rc = check_seqs(seq, 1, 0))) return rc;
+  if ((rc = check_layer(layer, sh)) || (rc = check_seqs(seq, 1, 0))) return rc;
+  if (sh.i4) return STV_ERR_UNIMPLEMENTED;  // the inspection reads the 3-bit groups
   if (!q_row || !dots || q_head < 0 || q_head >= sh.hq) return STV_ERR_INVALID_ARG;
   if (tok_begin < 0 || tok_end < tok_begin || (int64_t)tok_end > (int64_t)seq->n_pages * kPageTok)
     return STV_ERR_INVALID_ARG;

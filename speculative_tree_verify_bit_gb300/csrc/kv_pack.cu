@@ -32,9 +32,66 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ 
   append_row_channel(__half2float(p.k[src]), __half2float(p.v[src]), hb, slot, c);
 }
 
+// The int4 per-token-head cache (include/stv.h, group 256): one CTA per
+// (row, KV head), thread = channel.  The scale is fp16(max|x| / 7) over the
+// whole row: an IEEE single division whose result is never within rounding
+// of an fp16 midpoint (m / 7 with m an fp16 value is at least 1/7 of a
+// half-ulp away from one), so rounding it to fp16 equals rounding m / 7
+// directly.  K: a word holds 8 channels, OR-reduced over 8 lanes; V: a word
+// holds one channel's codes for 8 tokens, read-modify-written with atomics
+// (rows appended in the same launch may share it; their nibbles differ).
+__global__ void __launch_bounds__(256) kv_append_i4_kernel(const __grid_constant__ AppendParams p) {
+  const int row = blockIdx.x / p.hkv, h = blockIdx.x % p.hkv;
+  const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
+  __shared__ float red[2][kHeadDim / 32];
+  const int s = __ldg(p.row_seq + row), pos = __ldg(p.row_pos + row);
+  if (s < 0 || s >= p.n_seqs || pos < 0) {
+    if (c == 0) report(p.status, STV_DEV_BAD_ROW);
+    return;
+  }
+  uint8_t* hb = const_cast<uint8_t*>(head_block(p.seq[s], p.pool, p.page_bytes, p.pool_pages, pos, h,
+                                                c == 0 ? p.status : nullptr, kI4HeadBytes));
+  if (!hb) return;
+  const int slot = pos & (kPageTok - 1);
+  const int64_t src = ((int64_t)row * p.hkv + h) * kHeadDim + c;
+  const float xk = __half2float(p.k[src]), xv = __half2float(p.v[src]);
+  const float mk = warp_max(fabsf(xk)), mv = warp_max(fabsf(xv));
+  if (lane == 0) {
+    red[0][warp] = mk;
+    red[1][warp] = mv;
+  }
+  __syncthreads();
+  float m0 = 0.f, m1 = 0.f;
+#pragma unroll
+  for (int w = 0; w < kHeadDim / 32; ++w) {
+    m0 = fmaxf(m0, red[0][w]);
+    m1 = fmaxf(m1, red[1][w]);
+  }
+  const __half sk = __float2half_rn(__fdiv_rn(m0, 7.f)), sv = __float2half_rn(__fdiv_rn(m1, 7.f));
+  // K: channel c is element c % 8 of word c / 8
+  uint32_t kw = (uint32_t)quant_code_i4(xk, __half2float(sk)) << i4_pos(c & 7);
+  kw |= __shfl_xor_sync(0xffffffffu, kw, 1);
+  kw |= __shfl_xor_sync(0xffffffffu, kw, 2);
+  kw |= __shfl_xor_sync(0xffffffffu, kw, 4);
+  if ((c & 7) == 0) *reinterpret_cast<uint32_t*>(hb + kI4OffKCodes + slot * 128 + (c >> 3) * 4) = kw;
+  // V: token `slot` is element slot % 8 of channel c's word for its 8 tokens
+  const int tile = slot / kTileTok, within = slot % kTileTok;
+  uint32_t* wp = reinterpret_cast<uint32_t*>(hb + kI4OffVCodes + tile * kI4VTileCodeBytes + c * 32 + (within / 8) * 4);
+  const int sh = i4_pos(within & 7);
+  atomicAnd(wp, ~(15u << sh));
+  atomicOr(wp, (uint32_t)quant_code_i4(xv, __half2float(sv)) << sh);
+  if (c == 0) {
+    *reinterpret_cast<__half*>(hb + kI4OffKScales + slot * 2) = sk;
+    *reinterpret_cast<__half*>(hb + kI4OffVScales + slot * 2) = sv;
+  }
+}
+
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t s) {
   if (p.n_rows == 0) return cudaSuccess;
-  kv_append_kernel<<<p.n_rows * p.hkv, 256, 0, s>>>(p);
+  if (p.i4)
+    kv_append_i4_kernel<<<p.n_rows * p.hkv, 256, 0, s>>>(p);
+  else
+    kv_append_kernel<<<p.n_rows * p.hkv, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -136,8 +193,93 @@ __global__ void __launch_bounds__(256) kv_commit_kernel(const __grid_constant__ 
   if (leader && p.ctx_dev) p.ctx_dev[s] += n;
 }
 
+// kv_commit for the int4 per-token-head cache: the same protocol as above
+// (validate the path, read every source row, then write), moving each row's
+// K codes and both scales whole and its V code channel by channel.
+__global__ void __launch_bounds__(256) kv_commit_i4_kernel(const __grid_constant__ CommitParams p) {
+  int b = blockIdx.x;
+  const int h = b % p.hkv;
+  b /= p.hkv;
+  const int layer = b % p.n_layers;
+  const int s = b / p.n_layers;
+  const int tid = threadIdx.x;
+  const bool leader = (layer == 0 && h == 0 && tid == 0);
+
+  __shared__ int path_s[kMaxT];
+  __shared__ int n_s, ok_s;
+  __shared__ __align__(16) uint8_t krow[kMaxT][128];  // K codes
+  __shared__ __align__(4) __half scl[kMaxT][2];       // K and V scales
+  __shared__ uint8_t vcode[kMaxT][kHeadDim];
+
+  if (tid == 0) {
+    int n = __ldg(p.n_commit + s);
+    int ok = (n >= 1 && n <= p.T);
+    int prev = -1;
+    for (int i = 0; ok && i < n; ++i) {
+      int x = __ldg(p.path + (int64_t)s * p.T + i);
+      path_s[i] = x;
+      if ((i == 0 && x != 0) || x <= prev || x >= p.T) ok = 0;
+      prev = x;
+    }
+    n_s = n;
+    ok_s = ok;
+  }
+  __syncthreads();
+  if (!ok_s) {
+    if (leader) report(p.status, STV_DEV_BAD_COMMIT);
+    return;
+  }
+  const int n = n_s;
+  const SeqDesc& sd = p.seq[s];
+  const uint8_t* pool = p.pools[layer];
+  const int32_t pool_pages = p.pool_pages[layer];
+
+  for (int i = 0; i < n; ++i) {
+    const int64_t src = (int64_t)sd.ctx + path_s[i];
+    const uint8_t* hb =
+        head_block(sd, pool, p.page_bytes, pool_pages, src, h, tid == 0 ? p.status : nullptr, kI4HeadBytes);
+    if (!hb) {
+      if (tid == 0) ok_s = 0;
+      continue;
+    }
+    const int slot = (int)(src & (kPageTok - 1)), tile = slot / kTileTok, within = slot % kTileTok;
+    if (tid < 8)
+      reinterpret_cast<uint4*>(krow[i])[tid] = reinterpret_cast<const uint4*>(hb + kI4OffKCodes + slot * 128)[tid];
+    else if (tid == 8)
+      scl[i][0] = *reinterpret_cast<const __half*>(hb + kI4OffKScales + slot * 2);
+    else if (tid == 9)
+      scl[i][1] = *reinterpret_cast<const __half*>(hb + kI4OffVScales + slot * 2);
+    const uint32_t w =
+        *reinterpret_cast<const uint32_t*>(hb + kI4OffVCodes + tile * kI4VTileCodeBytes + tid * 32 + (within / 8) * 4);
+    vcode[i][tid] = (uint8_t)((w >> i4_pos(within & 7)) & 15u);
+  }
+  __syncthreads();
+  if (!ok_s) return;
+
+  for (int i = 0; i < n; ++i) {
+    const int64_t dst = (int64_t)sd.ctx + i;
+    uint8_t* hb = const_cast<uint8_t*>(head_block(sd, pool, p.page_bytes, pool_pages, dst, h, nullptr, kI4HeadBytes));
+    if (!hb) continue;
+    const int slot = (int)(dst & (kPageTok - 1)), tile = slot / kTileTok, within = slot % kTileTok;
+    if (tid < 8)
+      reinterpret_cast<uint4*>(hb + kI4OffKCodes + slot * 128)[tid] = reinterpret_cast<const uint4*>(krow[i])[tid];
+    else if (tid == 8)
+      *reinterpret_cast<__half*>(hb + kI4OffKScales + slot * 2) = scl[i][0];
+    else if (tid == 9)
+      *reinterpret_cast<__half*>(hb + kI4OffVScales + slot * 2) = scl[i][1];
+    // Channel `tid` owns its V words in this head: plain read-modify-write.
+    uint32_t* wp = reinterpret_cast<uint32_t*>(hb + kI4OffVCodes + tile * kI4VTileCodeBytes + tid * 32 + (within / 8) * 4);
+    const int sh = i4_pos(within & 7);
+    *wp = (*wp & ~(15u << sh)) | ((uint32_t)vcode[i][tid] << sh);
+  }
+  if (leader && p.ctx_dev) p.ctx_dev[s] += n;
+}
+
 cudaError_t launch_kv_commit(const CommitParams& p, cudaStream_t s) {
-  kv_commit_kernel<<<p.n_seqs * p.n_layers * p.hkv, 256, 0, s>>>(p);
+  if (p.i4)
+    kv_commit_i4_kernel<<<p.n_seqs * p.n_layers * p.hkv, 256, 0, s>>>(p);
+  else
+    kv_commit_kernel<<<p.n_seqs * p.n_layers * p.hkv, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -16,7 +16,8 @@ __device__ __forceinline__ void report(int32_t* status, int bit) {
 // Base of KV head h's block in the page holding token `tok` of sequence s,
 // or nullptr (and STV_DEV_BAD_PAGE) when the table or the pool is exceeded.
 __device__ __forceinline__ const uint8_t* head_block(const SeqDesc& sd, const uint8_t* pool, int64_t page_bytes,
-                                                     int32_t pool_pages, int64_t tok, int h, int32_t* status) {
+                                                     int32_t pool_pages, int64_t tok, int h, int32_t* status,
+                                                     int head_bytes = kHeadBytes) {
   int64_t lp = tok >> 8;
   if (tok < 0 || lp >= sd.n_pages) {
     report(status, STV_DEV_BAD_PAGE);
@@ -27,7 +28,7 @@ __device__ __forceinline__ const uint8_t* head_block(const SeqDesc& sd, const ui
     report(status, STV_DEV_BAD_PAGE);
     return nullptr;
   }
-  return pool + (int64_t)page * page_bytes + (int64_t)h * kHeadBytes;
+  return pool + (int64_t)page * page_bytes + (int64_t)h * head_bytes;
 }
 
 // Bit b of code i of a 32-code block: word and bit index (the layout stated
@@ -105,18 +106,17 @@ __device__ __forceinline__ float warp_max(float x) {
   return x;
 }
 
-// 3-bit code of x for scale s (the quantizer of include/stv.h):
-// clamp(rne(x / s) + 4, 0, 7), exactly, without a division.  q = x * (1/s)
-// from the approximate reciprocal is within far less than 1/2 of x / s
-// (|x / s| <= 8 here), so c = rint(q) is rne(x / s) or next to it, and only
-// when x / s lies near a half-integer.  The residual d = x - c s is exact:
-// either c = 0 (d = x) or |x| >= s/2, and then x and c s (fp16 values times
-// integers of at most 4 bits) are a few binades apart, so d needs at most
-// about 15 significant bits.  d against +-s/2 (exact) settles the rounding,
-// ties to the even integer.  s = fp16(max|x| / 4) is a normal fp32 value or
-// zero, so the reciprocal's flush-to-zero mode never applies.
-__device__ __forceinline__ int quant_code(float x, float s) {
-  if (s == 0.f) return 4;
+// rne(x / s) for s > 0, exactly, without a division (both quantizers of
+// include/stv.h; |x / s| <= 11 for them).  q = x * (1/s) from the
+// approximate reciprocal is within far less than 1/2 of x / s, so c = rint(q)
+// is rne(x / s) or next to it, and only when x / s lies near a half-integer.
+// The residual d = x - c s is exact: either c = 0 (d = x) or |x| >= s/2, and
+// then x and c s (fp16 values times integers of at most 4 bits) are a few
+// binades apart, so d needs at most about 16 significant bits.  d against
+// +-s/2 (exact) settles the rounding, ties to the even integer.  s is an fp16
+// value, so a normal fp32 value, and the reciprocal's flush-to-zero mode
+// never applies.
+__device__ __forceinline__ int rne_quotient(float x, float s) {
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
   int c = __float2int_rn(x * r);
@@ -124,7 +124,51 @@ __device__ __forceinline__ int quant_code(float x, float s) {
   const bool odd = (c & 1) != 0;
   if (d > hs || (d == hs && odd)) c += 1;        // closer to c + 1, or a tie with odd c
   else if (d < -hs || (d == -hs && odd)) c -= 1;  // closer to c - 1, or a tie with odd c
-  return min(max(c + 4, 0), 7);
+  return c;
+}
+
+// 3-bit code of x for scale s: clamp(rne(x / s) + 4, 0, 7); 4 when s == 0.
+__device__ __forceinline__ int quant_code(float x, float s) {
+  if (s == 0.f) return 4;
+  return min(max(rne_quotient(x, s) + 4, 0), 7);
+}
+
+// int4 code u = c + 8 of x for scale s: c = clamp(rne(x / s), -8, 7); 8 when
+// s == 0 (the int4 per-token-head cache of include/stv.h).
+__device__ __forceinline__ int quant_code_i4(float x, float s) {
+  if (s == 0.f) return 8;
+  return min(max(rne_quotient(x, s), -8), 7) + 8;
+}
+
+// Bit position of element e (0..7) of an int4 word: 4 * (e / 2), plus 16
+// for odd e, so that one AND/OR per pair makes an fp16 pair (below).
+__device__ __forceinline__ int i4_pos(int e) { return ((e & 1) ? 16 : 0) + 4 * (e >> 1); }
+
+// Decode four int4 words (32 elements, pairs (2m, 2m+1) in order) into 16
+// fp16 pairs of the signed codes c = u - 8.  Elements 0/1 of a word drop into
+// the mantissas of 1024 (lowest bit weighs 1) and elements 2/3 into those of
+// 64 (bits 4..7 weigh 1) with one AND/OR each, giving base + u exactly; the
+// upper byte's elements 4..7 do the same after one shift.  Subtracting
+// base + 8 is exact, so every code comes out exact.
+__device__ __forceinline__ void decode_i4_codes_h2(const uint32_t (&w)[4], __half2 (&out)[16]) {
+  const __half2 b1032 = u32_as_h2(0x64086408u);  // 1032
+  const __half2 b72 = u32_as_h2(0x54805480u);    // 72
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t x = w[j], xs = x >> 8;
+    out[4 * j + 0] = __hsub2(u32_as_h2((x & 0x000F000Fu) | 0x64006400u), b1032);
+    out[4 * j + 1] = __hsub2(u32_as_h2((x & 0x00F000F0u) | 0x54005400u), b72);
+    out[4 * j + 2] = __hsub2(u32_as_h2((xs & 0x000F000Fu) | 0x64006400u), b1032);
+    out[4 * j + 3] = __hsub2(u32_as_h2((xs & 0x00F000F0u) | 0x54005400u), b72);
+  }
+}
+
+// The same, times a scale per pair: scale * c with one fp16 rounding.
+template <typename ScaleFn>
+__device__ __forceinline__ void decode_i4_block_h2(const uint32_t (&w)[4], ScaleFn scale, __half2 (&out)[16]) {
+  decode_i4_codes_h2(w, out);
+#pragma unroll
+  for (int m = 0; m < 16; ++m) out[m] = __hmul2(out[m], scale(m));
 }
 
 // One channel of one (row, KV head): called by 256 threads, thread c =

@@ -32,6 +32,19 @@ constexpr int kKTileCodeBytes = kTileTok * 96;                     // 6144
 constexpr int kKTileScaleBytes = kTileTok * 16;                    // 1024
 static_assert(kHeadBytes == STV_HEAD_BLOCK_BYTES, "layout");
 
+// The int4 per-token-head format (group 256; see include/stv.h).
+constexpr int kGroupI4 = 256;
+constexpr int kI4OffKCodes = 0;
+constexpr int kI4OffKScales = kPageTok * 128;                 // 32768
+constexpr int kI4OffVCodes = kI4OffKScales + kPageTok * 2;    // 33280
+constexpr int kI4OffVScales = kI4OffVCodes + kPageTok * 128;  // 66048
+constexpr int kI4HeadBytes = kI4OffVScales + kPageTok * 2;    // 66560
+constexpr int kI4KTileCodeBytes = kTileTok * 128;             // 8192: one 64-token tile
+constexpr int kI4KTileScaleBytes = kTileTok * 2;              // 128
+constexpr int kI4VTileCodeBytes = kHeadDim * 32;              // 8192
+constexpr int kI4VTileScaleBytes = kTileTok * 2;              // 128
+static_assert(kI4HeadBytes == STV_HEAD_BLOCK_BYTES_INT4, "layout");
+
 struct SeqDesc {
   const int32_t* page_table;
   int32_t n_pages;
@@ -57,6 +70,7 @@ struct WsLayout {
 
 struct ShapeInfo {
   int hq, hkv, G, T, R;  // R = T * G rows per KV head
+  int i4;                // 1: the int4 per-token-head cache (group 256)
 };
 
 // Parameters of one verify launch (passed by value; < 4 KB).
@@ -81,6 +95,7 @@ struct VerifyParams {
   // sequence s goes to position ctx_s + i.
   const __half* k_tree;
   const __half* v_tree;
+  int i4;  // int4 per-token-head cache
   int32_t* status;
 };
 
@@ -105,6 +120,7 @@ struct AppendParams {
   const int32_t* row_seq;
   const int32_t* row_pos;
   int n_rows;
+  int i4;  // int4 per-token-head cache
   int32_t* status;
 };
 
@@ -118,6 +134,7 @@ struct CommitParams {
   const int32_t* n_commit;
   const int32_t* path;
   int32_t* ctx_dev;
+  int i4;  // int4 per-token-head cache
   int32_t* status;
 };
 

@@ -43,6 +43,38 @@ constexpr int kStageBytes = kKTileCodeBytes + kKTileScaleBytes + kVTileCodeBytes
 constexpr int kOperandBytes = 32768;  // one K or V^T fp16 tile
 constexpr int kVBuffers = 3;  // V^T tiles in flight: unpack may run two P.V products ahead
 constexpr int kSmemBytes = 1024 /*align slack*/ + (2 + kVBuffers) * kOperandBytes + kStages * kStageBytes + 1024 /*barriers etc*/;
+
+// The cache format's tile arrays (include/stv.h): the pages' 3-bit cache, or
+// the int4 per-token-head cache, whose larger stage leaves room for 3 stages.
+// The int4 K scale is one per key for the whole head, so it factors out of
+// Q.K: the K operand holds the exact codes and the softmax multiplies key j's
+// score by its scale in fp32 (no fp16 rounding of scale * code on the score
+// path).  The unpack warps hand the scales over in slot i % kKScaleSlots:
+// unpacking tile i + 4 waits for QK(i + 2) to finish, which the MMA warp
+// issues only after the softmax of tile i has arrived on p_full, so a slot is
+// never rewritten while it is read.
+constexpr int kKScaleSlots = 4;
+template <bool kI4>
+struct Fmt {
+  static constexpr int stages = kStages;
+  static constexpr int head = kHeadBytes;
+  static constexpr int off_kc = kOffKCodes, off_ks = kOffKScales, off_vc = kOffVCodes, off_vs = kOffVScales;
+  static constexpr int kc = kKTileCodeBytes, ks = kKTileScaleBytes, vc = kVTileCodeBytes, vs = kVTileScaleBytes;
+  static constexpr int stage = kStageBytes;
+  static constexpr int smem = kSmemBytes;
+};
+template <>
+struct Fmt<true> {
+  static constexpr int stages = 3;
+  static constexpr int head = kI4HeadBytes;
+  static constexpr int off_kc = kI4OffKCodes, off_ks = kI4OffKScales, off_vc = kI4OffVCodes, off_vs = kI4OffVScales;
+  static constexpr int kc = kI4KTileCodeBytes, ks = kI4KTileScaleBytes, vc = kI4VTileCodeBytes, vs = kI4VTileScaleBytes;
+  static constexpr int stage = kc + ks + vc + vs;  // 16640
+  // + the per-key K scales of the last kKScaleSlots tiles, as fp32
+  static constexpr int smem = 1024 + (2 + kVBuffers) * kOperandBytes + stages * stage + 1024 + kKScaleSlots * kTileTok * 4;
+};
+static_assert(Fmt<true>::stages <= kStages, "barrier arrays");
+static_assert(Fmt<true>::smem <= 232448, "shared memory per CTA");
 constexpr uint32_t kWaitLimit = 1u << 20;   // try_wait calls before a wait gives up
 constexpr uint32_t kSuspendHintNs = 20000;  // per try_wait
 constexpr float kLog2e = 1.4426950408889634f;
@@ -68,6 +100,8 @@ struct Bars {
   int abort;
   uint32_t anc[kMaxT];
 };
+
+static_assert(sizeof(Bars) <= 1024, "barrier block");
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
@@ -210,8 +244,9 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 
 // kAppend: the round's tree rows are packed into the cache by this launch
 // (stv_append_verify_attn); the plain instantiation carries none of that code.
-template <bool kAppend>
+template <bool kAppend, bool kI4>
 __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_constant__ VerifyParams p) {
+  using F = Fmt<kI4>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment of the operand tiles (the swizzle works on address bits).
   const uint32_t base_u32 = su32(smem_raw);
@@ -219,7 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
   uint8_t* const kdeq0 = smem;                      // K tiles: kdeq0 + b * kOperandBytes
   uint8_t* const vdeq0 = smem + 2 * kOperandBytes;  // V^T tiles: vdeq0 + b * kOperandBytes
   uint8_t* ring = smem + (2 + kVBuffers) * kOperandBytes;
-  Bars* bars = reinterpret_cast<Bars*>(ring + kStages * kStageBytes);
+  Bars* bars = reinterpret_cast<Bars*>(ring + F::stages * F::stage);
+  float* const kscale = reinterpret_cast<float*>(ring + F::stages * F::stage + 1024);  // int4 only
   volatile int* abort_flag = &bars->abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -237,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
 
   // ---- set-up ----
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < F::stages; ++i) {
       mbar_init(&bars->raw_full[i], 1);
       mbar_init(&bars->raw_empty[i], 8);
     }
@@ -291,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
       int issued = 0;
       bool tree_ready = !kAppend;
       for (int i = 0; i < n_tiles; ++i) {
-        const int st = i % kStages;
-        if (!wait1(&bars->raw_empty[st], ((i / kStages) & 1) ^ 1, abort_flag)) break;
+        const int st = i % F::stages;
+        if (!wait1(&bars->raw_empty[st], ((i / F::stages) & 1) ^ 1, abort_flag)) break;
         const int key0 = tok0 + i * kTileTok;
         // a tile holding tree keys is copied only after the unpack warps have
         // packed them (their global writes are fenced for the async proxy)
@@ -306,23 +342,21 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
           report(p.status, STV_DEV_BAD_PAGE);
           page = 0;  // read a valid page; the result is flagged as garbage
         }
-        const uint8_t* hb = p.pool + (int64_t)page * p.page_bytes + (int64_t)h * kHeadBytes;
+        const uint8_t* hb = p.pool + (int64_t)page * p.page_bytes + (int64_t)h * F::head;
         const int t = (key0 & (kPageTok - 1)) / kTileTok;
-        uint8_t* dst = ring + st * kStageBytes;
+        uint8_t* dst = ring + st * F::stage;
         uint64_t* bar = &bars->raw_full[st];
-        mbar_expect_tx(bar, kStageBytes);
-        bulk_g2s(dst, hb + kOffKCodes + t * kKTileCodeBytes, kKTileCodeBytes, bar);
-        bulk_g2s(dst + kKTileCodeBytes, hb + kOffKScales + t * kKTileScaleBytes, kKTileScaleBytes, bar);
-        bulk_g2s(dst + kKTileCodeBytes + kKTileScaleBytes, hb + kOffVCodes + t * kVTileCodeBytes, kVTileCodeBytes,
-                 bar);
-        bulk_g2s(dst + kKTileCodeBytes + kKTileScaleBytes + kVTileCodeBytes, hb + kOffVScales + t * kVTileScaleBytes,
-                 kVTileScaleBytes, bar);
+        mbar_expect_tx(bar, F::stage);
+        bulk_g2s(dst, hb + F::off_kc + t * F::kc, F::kc, bar);
+        bulk_g2s(dst + F::kc, hb + F::off_ks + t * F::ks, F::ks, bar);
+        bulk_g2s(dst + F::kc + F::ks, hb + F::off_vc + t * F::vc, F::vc, bar);
+        bulk_g2s(dst + F::kc + F::ks + F::vc, hb + F::off_vs + t * F::vs, F::vs, bar);
         issued = i + 1;
       }
       // No copy may still be landing when the CTA exits.
-      for (int i = max(0, issued - kStages); i < issued; ++i) {
+      for (int i = max(0, issued - F::stages); i < issued; ++i) {
         volatile int never = 0;
-        wait1(&bars->raw_full[i % kStages], (i / kStages) & 1, &never);
+        wait1(&bars->raw_full[i % F::stages], (i / F::stages) & 1, &never);
       }
     }
   } else if (warp == 1) {
@@ -430,6 +464,21 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
       tmem_ld32(lane_addr + kColS0 + 64 * b + 32, sb);
       tmem_wait_ld(sa);
       tmem_wait_ld(sb);
+      if constexpr (kI4) {  // S = (Q.codes) * per-key scale, in fp32
+        const float4* ksc = reinterpret_cast<const float4*>(kscale + (i % kKScaleSlots) * kTileTok);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float4 x = ksc[e], y = ksc[8 + e];
+          sa[4 * e] = __float_as_uint(__uint_as_float(sa[4 * e]) * x.x);
+          sa[4 * e + 1] = __float_as_uint(__uint_as_float(sa[4 * e + 1]) * x.y);
+          sa[4 * e + 2] = __float_as_uint(__uint_as_float(sa[4 * e + 2]) * x.z);
+          sa[4 * e + 3] = __float_as_uint(__uint_as_float(sa[4 * e + 3]) * x.w);
+          sb[4 * e] = __float_as_uint(__uint_as_float(sb[4 * e]) * y.x);
+          sb[4 * e + 1] = __float_as_uint(__uint_as_float(sb[4 * e + 1]) * y.y);
+          sb[4 * e + 2] = __float_as_uint(__uint_as_float(sb[4 * e + 2]) * y.z);
+          sb[4 * e + 3] = __float_as_uint(__uint_as_float(sb[4 * e + 3]) * y.w);
+        }
+      }
       const int key0 = tok0 + i * kTileTok;
       if (key0 + kTileTok > sd.ctx || key0 + kTileTok > tok1) {
         // Visibility of the tile's 64 keys as one bit mask: context keys,
@@ -612,17 +661,38 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
       }
     }
     for (int i = 0; i < n_tiles; ++i) {
-      const int st = i % kStages, b = i & 1;
-      const uint8_t* stage = ring + st * kStageBytes;
-      const uint32_t pr_raw = probe(&bars->raw_full[st], (i / kStages) & 1);
+      const int st = i % F::stages, b = i & 1;
+      const uint8_t* stage = ring + st * F::stage;
+      const uint32_t pr_raw = probe(&bars->raw_full[st], (i / F::stages) & 1);
       const uint32_t pr_kd = probe(&bars->kd_empty[b], ((i >> 1) & 1) ^ 1);
       const int vb = i % kVBuffers;
       const uint32_t pr_vd = probe(&bars->vd_empty[vb], ((i / kVBuffers) & 1) ^ 1);
-      if (!settle(&bars->raw_full[st], (i / kStages) & 1, pr_raw, abort_flag)) break;
+      if (!settle(&bars->raw_full[st], (i / F::stages) & 1, pr_raw, abort_flag)) break;
       const int key0 = tok0 + i * kTileTok;
       // ---- K: key kj, groups 2*kcb and 2*kcb+1 -> one 128-byte swizzled row ----
       if (!settle(&bars->kd_empty[b], ((i >> 1) & 1) ^ 1, pr_kd, abort_flag)) break;
-      {
+      if constexpr (kI4) {
+        // int4: key kj's 64 channels are 8 words, stored as exact codes; the
+        // key's one scale goes to the softmax (zero for keys past the range,
+        // whose stale bytes could hold anything)
+        const uint4* wq = reinterpret_cast<const uint4*>(stage + kj * 128 + kcb * 32);
+        const uint4 a0 = wq[0], a1 = wq[1];
+        if (kcb == 0) {
+          const float sk = __half2float(*reinterpret_cast<const __half*>(stage + F::kc + kj * 2));
+          kscale[(i % kKScaleSlots) * kTileTok + kj] = key0 + kj < tok1 ? sk : 0.f;
+        }
+        const uint32_t krow = su32(kdeq0) + b * kOperandBytes + kcb * 8192 + sw128_row(kj);
+        __half2 out[16];
+        const uint32_t w0[4] = {a0.x, a0.y, a0.z, a0.w}, w1[4] = {a1.x, a1.y, a1.z, a1.w};
+        decode_i4_codes_h2(w0, out);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          st_shared_v4(sw128_chunk(krow, q4), out[4 * q4], out[4 * q4 + 1], out[4 * q4 + 2], out[4 * q4 + 3]);
+        decode_i4_codes_h2(w1, out);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          st_shared_v4(sw128_chunk(krow, 4 + q4), out[4 * q4], out[4 * q4 + 1], out[4 * q4 + 2], out[4 * q4 + 3]);
+      } else {
         const uint2* wv = reinterpret_cast<const uint2*>(stage + kj * 96 + kcb * 24);
         const uint2 w01 = wv[0], w23 = wv[1], w45 = wv[2];
         const __half2 sc2 = *reinterpret_cast<const __half2*>(stage + kKTileCodeBytes + kj * 16 + kcb * 4);
@@ -643,7 +713,41 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
       if (lane == 0) mbar_arrive(&bars->kd_full[b]);
       // ---- V: channel vch, 64 keys -> one 128-byte swizzled row of V^T ----
       if (!settle(&bars->vd_empty[vb], ((i / kVBuffers) & 1) ^ 1, pr_vd, abort_flag)) break;
-      {
+      if constexpr (kI4) {
+        // int4: channel vch's 64 keys are 8 words; the tile's 64 per-token
+        // scales, as 32 (key 2m, 2m+1) pairs, are the same for every channel
+        const uint4* wq = reinterpret_cast<const uint4*>(stage + F::kc + F::ks + vch * 32);
+        const uint4 a0 = wq[0], a1 = wq[1];
+        const uint4* sp = reinterpret_cast<const uint4*>(stage + F::kc + F::ks + F::vc);
+        const int live = tok1 - key0;  // keys at or beyond this are zeroed
+        const uint32_t vrow = su32(vdeq0) + vb * kOperandBytes + sw128_row(vch);
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          uint32_t sc[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 x = sp[blk * 4 + q];
+            sc[4 * q] = x.x;
+            sc[4 * q + 1] = x.y;
+            sc[4 * q + 2] = x.z;
+            sc[4 * q + 3] = x.w;
+          }
+          __half2 out[16];
+          const uint32_t w[4] = {blk ? a1.x : a0.x, blk ? a1.y : a0.y, blk ? a1.z : a0.z, blk ? a1.w : a0.w};
+          decode_i4_block_h2(w, [&](int m) { return u32_as_h2(sc[m]); }, out);
+          if (live < 64) {
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+              const int k0 = blk * 32 + 2 * m;
+              if (k0 >= live) out[m] = __floats2half2_rn(0.f, 0.f);
+              else if (k0 + 1 >= live) out[m] = __halves2half2(__low2half(out[m]), __float2half_rn(0.f));
+            }
+          }
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            st_shared_v4(sw128_chunk(vrow, blk * 4 + q4), out[4 * q4], out[4 * q4 + 1], out[4 * q4 + 2], out[4 * q4 + 3]);
+        }
+      } else {
         const uint2* wv = reinterpret_cast<const uint2*>(stage + kKTileCodeBytes + kKTileScaleBytes + vch * 24);
         const uint2 w01 = wv[0], w23 = wv[1], w45 = wv[2];
         // this channel's group: 64 key scales, as 32 (key 2m, 2m+1) pairs
@@ -703,10 +807,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
 
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s) {
   const bool append = p.k_tree != nullptr && p.v_tree != nullptr;
-  auto kernel = append ? verify_tc_kernel<true> : verify_tc_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  // the fused append packs the 3-bit cache only (the host refuses it for int4)
+  auto kernel = p.i4 ? verify_tc_kernel<false, true>
+                     : (append ? verify_tc_kernel<true, false> : verify_tc_kernel<false, false>);
+  const int smem = p.i4 ? Fmt<true>::smem : Fmt<false>::smem;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kernel<<<p.n_units, kThreads, kSmemBytes, s>>>(p);
+  kernel<<<p.n_units, kThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -20,7 +20,7 @@ class Round:
     """Inputs of one layer's round: contexts, trees, fp16 K/V/Q, page tables."""
 
     def __init__(self, ctx, t_nodes, seed, hq=24, hkv=4, tree="random", p_accept=0.7, max_depth=8,
-                 device="cuda", extra_pages=1, parents=None):
+                 device="cuda", extra_pages=1, parents=None, group=32):
         self.ctx = list(ctx)
         self.n_seqs = len(self.ctx)
         self.T, self.hq, self.hkv = t_nodes, hq, hkv
@@ -60,11 +60,12 @@ class Round:
         self.row_seq = np.concatenate([np.full(c + t_nodes, s, np.int32) for s, c in enumerate(self.ctx)])
         self.row_pos = np.concatenate([np.arange(c + t_nodes, dtype=np.int32) for c in self.ctx])
         self.q = workloads.q_rows(seed, self.n_seqs, t_nodes, hq, device=device).contiguous()
-        self.shape = stv.make_shape(hq, hkv)
+        self.group = group  # 32: the 3-bit cache; 256: the int4 per-token-head cache
+        self.shape = stv.make_shape(hq, hkv, group)
 
     # ---------------- GPU side ----------------
     def gpu_cache(self):
-        layer = stv.LayerCache.empty(self.pool_pages, self.hkv, device=self.device)
+        layer = stv.LayerCache.empty(self.pool_pages, self.hkv, device=self.device, group=self.group)
         self.seqs = [stv.Seq(torch.as_tensor(t, device=self.device), c) for t, c in zip(self.tables, self.ctx)]
         status = torch.zeros(1, dtype=torch.int32, device=self.device)
         stv.stv_kv_append_pack(self.shape, layer, self.seqs, self.k, self.v,
@@ -90,7 +91,7 @@ class Round:
 
     # ---------------- oracle side ----------------
     def oracle_cache(self):
-        cache = oracle.Cache(self.hkv, self.pool_pages)
+        cache = oracle.Cache(self.hkv, self.pool_pages, bits=4 if self.group == 256 else 3)
         oracle.kv_append(cache, self.tables, self.k.cpu().numpy(), self.v.cpu().numpy(), self.row_seq, self.row_pos)
         self.ocache = cache
         return cache
