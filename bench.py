@@ -46,17 +46,23 @@ METRIC = "verify-attn us/layer-round and HBM GB/s (% of roofline) at 32K and 262
 UNIT = "us/layer-round"
 
 
-def algorithmic_bytes_per_layer_round(ctx_list, t, hq=24, hkv=4):
-    """Packed KV streamed by verify (768 B codes + 128 B scales per token over
-    4 KV heads) plus Q in and O out."""
-    kv = sum(c + t for c in ctx_list) * hkv * (2 * 96 + 2 * 16)
+# Packed bytes per token and KV head, K + V: the 3-bit cache holds 96 B of
+# codes and 16 B of fp16 group scales for each; the int4 per-token-head cache
+# 128 B of codes and one 2 B scale.
+KV_FORMATS = {"bit3": (32, 2 * (96 + 16)), "int4": (256, 2 * (128 + 2))}
+
+
+def algorithmic_bytes_per_layer_round(ctx_list, t, hq=24, hkv=4, kv_format="bit3"):
+    """Packed KV streamed by verify (every visible key's bytes over all KV
+    heads) plus Q in and O out."""
+    kv = sum(c + t for c in ctx_list) * hkv * KV_FORMATS[kv_format][1]
     qo = len(ctx_list) * 2 * t * hq * 256 * 2
     return kv + qo
 
 
-def verify_kernel_bytes(ctx_list, t, hq=24, hkv=4):
+def verify_kernel_bytes(ctx_list, t, hq=24, hkv=4, kv_format="bit3"):
     """Bytes one verify launch must read: packed KV of every visible key and Q."""
-    return sum(c + t for c in ctx_list) * hkv * (2 * 96 + 2 * 16) + len(ctx_list) * t * hq * 256 * 2
+    return sum(c + t for c in ctx_list) * hkv * KV_FORMATS[kv_format][1] + len(ctx_list) * t * hq * 256 * 2
 
 
 def measured_peak():
@@ -356,13 +362,6 @@ def measure_prefill(dev, n: int = 32768, reps: int = 3, hq: int = 24, hkv: int =
             "bound": "tensor", "tflops": tflops, "peak_tflops": peak, "frac": tflops / peak, "peak_source": kind}
 
 
-def int4_verify_bytes(ctx_list, t, hq=24, hkv=4):
-    """Bytes one verify launch must read from the int4 per-token-head cache:
-    128 B of K codes + 2 B of K scale and the same for V per token and KV
-    head, for every visible key, and Q."""
-    return sum(c + t for c in ctx_list) * hkv * 2 * (128 + 2) + len(ctx_list) * t * hq * 256 * 2
-
-
 def measure_int4(w: workloads.Workload, p_accept: float, dev, path: str = "exact", reps: int = 10):
     """The same round over the int4 per-token-head cache (group 256): two
     layers resident, eager rounds with events around each verify launch; the
@@ -386,7 +385,7 @@ def measure_int4(w: workloads.Workload, p_accept: float, dev, path: str = "exact
         rounds.append(a.elapsed_time(b))
     st = int(r.status.item())
     v_us = statistics.median(times) * 1e3
-    vbytes = int4_verify_bytes(w.ctx, w.t_nodes, w.hq, w.hkv)
+    vbytes = verify_kernel_bytes(w.ctx, w.t_nodes, w.hq, w.hkv, "int4")
     peak, kind = measured_peak()
     gbs = vbytes / (v_us * 1e-6) / 1e9
     out = {"workload": w.name, "group": 256, "path": path, "verify_us_per_launch": v_us,
@@ -422,7 +421,8 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(dev)
     w = workloads.WORKLOADS[args.workload]
     p_accept = default_p_accept(args, w)
-    r = GpuRound(w, p_accept, dev, layers=args.layers, fuse_append=args.fuse_append)
+    r = GpuRound(w, p_accept, dev, layers=args.layers, fuse_append=args.fuse_append,
+                 group=KV_FORMATS[args.kv_format][0])
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -503,19 +503,20 @@ def run_gpu(args, rank, world):
     e2e_ms = e0.elapsed_time(e1)
 
     med_ms = statistics.median(round_ms)  # a round = one graph replay
-    lookup = measure_lookup(w, dev) if rank == 0 else None
-    prefill = measure_prefill(dev) if rank == 0 else None
-    int4 = measure_int4(w, p_accept, dev, args.path) if rank == 0 else None
+    extra = rank == 0 and not args.no_next_rows
+    lookup = measure_lookup(w, dev) if extra else None
+    prefill = measure_prefill(dev) if extra else None
+    int4 = measure_int4(w, p_accept, dev, args.path) if extra and args.kv_format == "bit3" else None
     med_ms, e2e_ms = max_over_ranks([med_ms, e2e_ms], dist, dev)
     layer_rounds = args.steps * r.L * world
     us_per_lr = us_per_layer_round(med_ms, r.L, world)
     e2e_us = e2e_ms * 1e3 / layer_rounds
-    bytes_lr = algorithmic_bytes_per_layer_round(w.ctx, w.t_nodes, w.hq, w.hkv)
-    vbytes = verify_kernel_bytes(w.ctx, w.t_nodes, w.hq, w.hkv)
+    bytes_lr = algorithmic_bytes_per_layer_round(w.ctx, w.t_nodes, w.hq, w.hkv, args.kv_format)
+    vbytes = verify_kernel_bytes(w.ctx, w.t_nodes, w.hq, w.hkv, args.kv_format)
     v_us = statistics.mean(verify_ms) * 1e3
     peak, peak_kind = measured_peak()
     achieved = vbytes / (v_us * 1e-6) / 1e9
-    traffic = load_traffic(args.workload, args.path)
+    traffic = load_traffic(args.workload, args.path, args.kv_format)
     return dict(rank=rank, us_per_lr=us_per_lr, e2e_us=e2e_us, bytes_lr=bytes_lr, v_us=v_us, vbytes=vbytes,
                 peak=peak, peak_kind=peak_kind, achieved=achieved, clocks=clk.summary(), status=st, h2d=h2d,
                 d2h=d2h, launches=r.launches_per_step(args.path) * args.steps, p_accept=p_accept, traffic=traffic,
@@ -523,7 +524,7 @@ def run_gpu(args, rank, world):
                 lookup=lookup, prefill=prefill, int4=int4)
 
 
-def load_traffic(workload, path):
+def load_traffic(workload, path, kv_format="bit3"):
     """DRAM bytes per verify launch from the committed ncu summary, or None
     when there is none for this workload or the verify kernel's source has
     changed since the counters were taken."""
@@ -537,7 +538,7 @@ def load_traffic(workload, path):
         src = os.path.join(ROOT, "speculative_tree_verify_bit_gb300", "csrc", "verify_tc.cu")
         if d.get("verify_tc_sha256") != hashlib.sha256(open(src, "rb").read()).hexdigest():
             return None
-        return d.get(f"{workload}/{path}")
+        return d.get(f"{workload}/{path}" + ("" if kv_format == "bit3" else f"/{kv_format}"))
     except Exception:
         return None
 
@@ -546,7 +547,7 @@ def load_traffic(workload, path):
 # CPU baseline: the fp64 oracle on the host cores, bounded sample
 # --------------------------------------------------------------------------
 
-def oracle_sample(w: workloads.Workload, n_rows: int, threads: int):
+def oracle_sample(w: workloads.Workload, n_rows: int, threads: int, kv_format: str = "bit3"):
     """Time the oracle on n_rows (node, Q head) rows of layer 0 over the full
     context; scale to microseconds per layer-round (all T * hq rows of every
     sequence).  The oracle's own cache is packed first (set-up, untimed)."""
@@ -556,7 +557,7 @@ def oracle_sample(w: workloads.Workload, n_rows: int, threads: int):
 
     T, hq, hkv = w.t_nodes, w.hq, w.hkv
     pool_pages, tables = workloads.page_tables_for(w)
-    cache = oracle.Cache(hkv, pool_pages)
+    cache = oracle.Cache(hkv, pool_pages, bits=3 if kv_format == "bit3" else 4)
     seed = workloads.layer_seed(w, 0)
     # the sample covers the largest sequence (the long-context share dominates)
     s = int(np.argmax(w.ctx))
@@ -576,7 +577,7 @@ def oracle_sample(w: workloads.Workload, n_rows: int, threads: int):
     keys_sampled = n_rows * (c + T)
     keys_all = sum(cc + T for cc in w.ctx) * T * hq
     us_per_lr = dt * 1e6 * keys_all / keys_sampled
-    sample = (f"oracle attention (fp64, exact path) for {n_rows} of {T * hq * w.n_seqs} (node, Q head) rows of "
+    sample = (f"oracle attention (fp64, exact path, {kv_format} cache) for {n_rows} of {T * hq * w.n_seqs} (node, Q head) rows of "
               f"layer 0 over the {c}-key context of sequence {s}, scaled by visible keys to one full layer-round")
     return us_per_lr, dt, sample
 
@@ -587,7 +588,8 @@ def arm_config(args, w: workloads.Workload, p_accept: float, world: int) -> dict
             "hq": w.hq, "hkv": w.hkv, "head_dim": 256, "path": args.path, "p_accept": p_accept,
             "l2": "inputs larger than L2 (16 layers of packed KV)", "parallelism": f"replicas{world}",
             "timing": "median over steps of one CUDA-graph replay of the round, CUDA events",
-            "append": "fused into verify" if args.fuse_append else "separate launch"}
+            "append": "fused into verify" if args.fuse_append else "separate launch",
+            "kv_format": {"bit3": "3-bit codes, fp16 scale per 32-group", "int4": "int4 codes, fp16 scale per token and KV head"}[args.kv_format]}
 
 
 def default_p_accept(args, w: workloads.Workload) -> float:
@@ -602,7 +604,7 @@ def run_reference(args):
         pass  # the oracle has no warm state; warm-up steps are not repeated
     n_rows = args.oracle_rows
     for _ in range(max(1, args.steps)):
-        v, dt, sample = oracle_sample(w, n_rows, threads)
+        v, dt, sample = oracle_sample(w, n_rows, threads, args.kv_format)
         vals.append(v)
         if dt > 60:
             break
@@ -635,8 +637,14 @@ def main():
                     help="append the tree rows inside the verify launch (stv_append_verify_attn) instead of "
                          "with their own launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv-format", default="bit3", choices=sorted(KV_FORMATS),
+                    help="cache format: the 3-bit cache (default) or the int4 per-token-head cache")
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="skip the lookup, prefill and int4 measurements (profiling captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.fuse_append and args.kv_format != "bit3":
+        ap.error("--fuse-append packs the 3-bit cache only")
 
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -657,7 +665,7 @@ def main():
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         threads = os.cpu_count() or 1
-        v, dt, sample = oracle_sample(w, args.oracle_rows, threads)
+        v, dt, sample = oracle_sample(w, args.oracle_rows, threads, args.kv_format)
         cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
     frac = res["achieved"] / res["peak"]
     line = {

@@ -590,7 +590,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
     // K: key and 64-channel column block.  Each group of 8 consecutive lanes
     // takes 8 different keys of one column block, so the 8 lanes of a
     // 128-bit store phase land on 8 different swizzled 16-byte positions.
-    const int kj = (ut >> 5) * 8 + (ut & 7), kcb = (ut >> 3) & 3;
+    // int4: a key's codes are one 128-byte row, so block kcb of every key
+    // sits in the same banks; a 128-bit load is served 8 lanes at a time,
+    // so the 8 lanes of each group take different blocks (kcb = j/2 + group,
+    // mod 4) and start at different halves (j mod 2), which makes the loads
+    // conflict-free while the stores keep 8 different keys per group.
+    const int kj = (ut >> 5) * 8 + (ut & 7);
+    const int kcb = kI4 ? (((ut & 7) >> 1) + ((ut >> 3) & 3)) & 3 : (ut >> 3) & 3;
     const int vch = ut;  // V: channel
     // ---- fused append: the tree rows whose keys fall in this unit's range ----
     // (a1 for KV head h; thread ut = channel, warp = 32-channel group, the
@@ -676,7 +682,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
         // key's one scale goes to the softmax (zero for keys past the range,
         // whose stale bytes could hold anything)
         const uint4* wq = reinterpret_cast<const uint4*>(stage + kj * 128 + kcb * 32);
-        const uint4 a0 = wq[0], a1 = wq[1];
+        const int hf = kj & 1;  // the half this lane loads first (see the lane mapping)
+        const uint4 x0 = wq[hf], x1 = wq[hf ^ 1];
+        const uint4 a0 = hf ? x1 : x0, a1 = hf ? x0 : x1;
         if (kcb == 0) {
           const float sk = __half2float(*reinterpret_cast<const __half*>(stage + F::kc + kj * 2));
           kscale[(i % kKScaleSlots) * kTileTok + kj] = key0 + kj < tok1 ? sk : 0.f;
@@ -716,8 +724,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
       if constexpr (kI4) {
         // int4: channel vch's 64 keys are 8 words; the tile's 64 per-token
         // scales, as 32 (key 2m, 2m+1) pairs, are the same for every channel
+        // channels 4..7 of each 8 start at the second half: conflict-free
         const uint4* wq = reinterpret_cast<const uint4*>(stage + F::kc + F::ks + vch * 32);
-        const uint4 a0 = wq[0], a1 = wq[1];
+        const int hf = (vch >> 2) & 1;
+        const uint4 x0 = wq[hf], x1 = wq[hf ^ 1];
+        const uint4 a0 = hf ? x1 : x0, a1 = hf ? x0 : x1;
         const uint4* sp = reinterpret_cast<const uint4*>(stage + F::kc + F::ks + F::vc);
         const int live = tok1 - key0;  // keys at or beyond this are zeroed
         const uint32_t vrow = su32(vdeq0) + vb * kOperandBytes + sw128_row(vch);
