@@ -666,6 +666,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
         if (lane == 0) mbar_arrive(&bars->tree_packed);
       }
     }
+    // Per tile: check the three barriers at once, unpack K then V, then one
+    // proxy fence and one arrival on each of kd_full, vd_full and raw_empty.
+    // (A fence and arrival after K as well cost about 7 % at 262K: the
+    // warp's fixed cost per tile is on the critical path.)  Holding K back
+    // until V is unpacked cannot deadlock: V(i) needs P.V(i-3), which the
+    // MMA warp issues after QK(i-2), whose K arrived one tile earlier.
     for (int i = 0; i < n_tiles; ++i) {
       const int st = i % F::stages, b = i & 1;
       const uint8_t* stage = ring + st * F::stage;
@@ -677,6 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
       const int key0 = tok0 + i * kTileTok;
       // ---- K: key kj, groups 2*kcb and 2*kcb+1 -> one 128-byte swizzled row ----
       if (!settle(&bars->kd_empty[b], ((i >> 1) & 1) ^ 1, pr_kd, abort_flag)) break;
+      if (!settle(&bars->vd_empty[vb], ((i / kVBuffers) & 1) ^ 1, pr_vd, abort_flag)) break;
       if constexpr (kI4) {
         // int4: key kj's 64 channels are 8 words, stored as exact codes; the
         // key's one scale goes to the softmax (zero for keys past the range,
@@ -716,11 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
         for (int q4 = 0; q4 < 4; ++q4)
           st_shared_v4(sw128_chunk(krow, 4 + q4), out[4 * q4], out[4 * q4 + 1], out[4 * q4 + 2], out[4 * q4 + 3]);
       }
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->kd_full[b]);
       // ---- V: channel vch, 64 keys -> one 128-byte swizzled row of V^T ----
-      if (!settle(&bars->vd_empty[vb], ((i / kVBuffers) & 1) ^ 1, pr_vd, abort_flag)) break;
       if constexpr (kI4) {
         // int4: channel vch's 64 keys are 8 words; the tile's 64 per-token
         // scales, as 32 (key 2m, 2m+1) pairs, are the same for every channel
@@ -798,6 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {
+        mbar_arrive(&bars->kd_full[b]);
         mbar_arrive(&bars->vd_full[vb]);
         mbar_arrive(&bars->raw_empty[st]);
       }
