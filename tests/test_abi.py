@@ -40,6 +40,8 @@ def test_status_strings(lib):
 
 def test_page_bytes_and_shape_validation(lib):
     assert stv.stv_page_bytes(stv.make_shape(24, 4)) == 229376
+    # the int4 per-token-head format (group 256): 4 heads x 66,560 B
+    assert stv.stv_page_bytes(stv.make_shape(24, 4, stv.GROUP_INT4)) == 4 * stv.HEAD_BLOCK_BYTES_INT4 == 266240
     for bad in (stv.stv_shape(24, 4, 128, 32, 256), stv.stv_shape(24, 5, 256, 32, 256),
                 stv.stv_shape(24, 4, 256, 16, 256), stv.stv_shape(24, 4, 256, 32, 128)):
         with pytest.raises(stv.StvError) as e:

@@ -45,3 +45,15 @@ def test_replicas_take_the_slowest_rank(world):
 def test_single_process_is_unchanged():
     assert bench.max_over_ranks([1.25, 7.0]) == [1.25, 7.0]
     assert bench.us_per_layer_round(3.2, 16, 1) == pytest.approx(200.0)
+
+
+def test_algorithmic_bytes_per_format():
+    """Per token and KV head, K + V: 3-bit 2 x (96 B codes + 16 B group
+    scales) = 224 B; int4 2 x (128 B codes + one 2 B scale) = 260 B; plus Q
+    (and O for the layer-round)."""
+    ctx, t, hq, hkv = [1000, 24], 16, 24, 4
+    q = len(ctx) * t * hq * 256 * 2
+    keys = (1000 + 16 + 24 + 16) * hkv
+    assert bench.verify_kernel_bytes(ctx, t, hq, hkv) == keys * 224 + q
+    assert bench.verify_kernel_bytes(ctx, t, hq, hkv, "int4") == keys * 260 + q
+    assert bench.algorithmic_bytes_per_layer_round(ctx, t, hq, hkv, "int4") == keys * 260 + 2 * q
