@@ -99,6 +99,23 @@ def test_full_size_sampled_rows(gpu, name):
         assert_attention_close(gather_heads(got, seqs, heads, r.T), want, f"{name}/{path}")
 
 
+@pytest.mark.parametrize("name,layers", [("tree32k", tuple(range(1, 16))), ("long262k", (7, 15))])
+def test_full_size_other_layers(gpu, name, layers):
+    """The other layers of the full-size workloads (layer 0 is above): every
+    layer at 32K and layers 7 and 15 at 262K, exact path, the first and last
+    Q head of each layer (all T nodes) against the oracle."""
+    w = workloads.WORKLOADS[name]
+    for layer in layers:
+        r = Round(list(w.ctx), w.t_nodes, seed=workloads.layer_seed(w, layer))
+        r.gpu_cache()
+        r.oracle_cache()
+        got = r.gpu_verify("exact").float().cpu().numpy()
+        heads = (0, r.hq - 1)
+        want = r.oracle_attention("exact", rows=head_rows((0,), heads, r.T)).reshape(-1, r.T, 256)
+        assert_attention_close(gather_heads(got, (0,), heads, r.T), want, f"{name} layer {layer}")
+        del r
+
+
 def test_int8_dots_bit_exact(gpu):
     r = Round([700], 16, seed=77)
     layer = r.gpu_cache()
