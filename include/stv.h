@@ -177,7 +177,10 @@ int stv_verify_workspace_bytes(const stv_shape* shape, const stv_seq* seqs, int 
  *           max|q|)) times the 3-bit K codes, scaled per group.
  * Key j < ctx is visible to every node; key ctx + k is visible to node i iff
  * k is i or an ancestor of i.  Scores are q . k / 16; softmax in fp32; P is
- * rounded to fp16 and P . V accumulates in fp32.  Writes partials into the
+ * rounded to fp16 and P . V accumulates in fp32.  On the int4 cache (group
+ * 256) a key's one scale covers the whole head, so Q is multiplied by the
+ * key's exact codes and the score by the key's scale in fp32 (both paths);
+ * V is dequantized to fp16 as on the 3-bit cache.  Writes partials into the
  * workspace; stv_split_combine produces the output.  The round's tree rows
  * must already be in the cache (stv_kv_append_pack).
  */
