@@ -114,3 +114,16 @@ def test_rows_per_kv_head_limit(lib):
     # T * G must stay <= 128: 32 nodes x 6 heads is rejected, 32 x 4 accepted
     assert _ws(stv.make_shape(24, 4), [10], [1], 32, 152)[0] == stv.STV_ERR_SHAPE_UNSUPPORTED
     assert _ws(stv.make_shape(16, 4), [10], [1], 32, 152)[0] == stv.STV_OK
+
+
+def test_int4_format_plans_like_the_3bit_cache(lib):
+    """The workspace and the split plan depend on the shape and the key
+    ranges, not on the cache format: group 256 sizes exactly as group 32, and
+    the host checks (T limit, pages) are the same."""
+    for ctxs, t in (([262144], 16), ([1024, 77, 4000], 7), ([0], 16)):
+        pages = [-(-(c + t) // 256) for c in ctxs]
+        rc3, b3 = _ws(stv.make_shape(24, 4), ctxs, pages, t, 152)
+        rc4, b4 = _ws(stv.make_shape(24, 4, stv.GROUP_INT4), ctxs, pages, t, 152)
+        assert rc3 == rc4 == 0 and b3 == b4
+    assert _ws(stv.make_shape(24, 4, stv.GROUP_INT4), [250], [1], 16, 152)[0] == stv.STV_ERR_INVALID_ARG
+    assert _ws(stv.make_shape(24, 4, stv.GROUP_INT4), [10], [1], 33, 152)[0] == stv.STV_ERR_SHAPE_UNSUPPORTED
