@@ -249,16 +249,21 @@ int stv_kv_commit(const stv_shape* shape, const stv_layer_cache* layers, int n_l
                   int32_t* dev_status, stv_stream_t stream);
 
 /*
- * Inspection entry point for the int8 path ("elpis" README, "Why fast":
- * 3-bit K codes as exact int8): the exact integer per-group dots
- * I_g = sum_{c in g} qi_c * (code_c - 4) of one Q row against keys
- * [tok_begin, tok_end) of one sequence, using the same int8 Q quantizer and
- * code decoding as STV_PATH_INT8.
- *  q_row: device fp16 [256]; dots: device int32 [tok_end - tok_begin][8].
+ * Inspection of the int8 path ("elpis" README, "Why fast": 3-bit K codes as
+ * exact int8): stv_verify_attn with STV_PATH_INT8 on one sequence that also
+ * writes out the per-group integer dots the verify kernel itself forms on
+ * the tensor cores, I_g = sum_{c in g} qi_c * (code_c - 4), for every key of
+ * [0, ctx + T) and every query row (whatever the tree mask says).
+ *  q, parent, t_nodes, workspace: as in stv_verify_attn (n_seqs = 1); the
+ *            workspace receives the same partials as stv_verify_attn.
+ *  dots:     device int32 [hkv][T * G][ctx + T][8]; row r of KV head h is
+ *            node r / G, Q head h * G + r % G (G = hq / hkv).
+ * STV_ERR_UNIMPLEMENTED on the int4 cache (group 256), whose int8 path has
+ * one group per key.
  */
-int stv_int8_qk_dots(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seq, const void* q_row,
-                     int q_head, int32_t tok_begin, int32_t tok_end, int32_t* dots, int32_t* dev_status,
-                     stv_stream_t stream);
+int stv_int8_qk_dots(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seq, const void* q,
+                     const int32_t* parent, int t_nodes, void* workspace, size_t ws_bytes, int32_t* dots,
+                     int32_t* dev_status, stv_stream_t stream);
 
 /*
  * Verify attention and split merge in one call, without a caller workspace

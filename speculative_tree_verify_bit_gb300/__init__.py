@@ -102,7 +102,7 @@ def load() -> ctypes.CDLL:
         lib.stv_kv_commit.restype = I
         lib.stv_kv_commit.argtypes = [P, P, I, P, I, I, P, P, P, P, P]
         lib.stv_int8_qk_dots.restype = I
-        lib.stv_int8_qk_dots.argtypes = [P, P, P, P, I, I32, I32, P, P, P]
+        lib.stv_int8_qk_dots.argtypes = [P, P, P, P, P, I, P, ctypes.c_size_t, P, P, P]
         lib.stv_prefill_workspace_bytes.restype = I
         lib.stv_prefill_workspace_bytes.argtypes = [P, P, I, P]
         lib.stv_prefill_attn.restype = I
@@ -303,16 +303,18 @@ def stv_kv_commit(shape, layers, seqs, t_nodes: int, n_commit, path, ctx_dev=Non
         _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
 
 
-def stv_int8_qk_dots(shape, layer: LayerCache, seq: Seq, q_row, q_head: int, tok_begin: int, tok_end: int, dots,
-                     dev_status=None, stream=None):
+def stv_int8_qk_dots(shape, layer: LayerCache, seq: Seq, q, parent, t_nodes: int, workspace, dots, dev_status=None,
+                     stream=None):
+    """The int8 verify of one sequence, also writing the kernel's own
+    per-group integer dots: dots int32 [hkv][T*G][ctx+T][8]."""
     import torch
 
     lc = layer.c()
-    sc = seq.c()
+    arr = _seq_array([seq])
     _check("stv_int8_qk_dots", load().stv_int8_qk_dots(
-        ctypes.byref(shape), ctypes.byref(lc), ctypes.byref(sc), _ptr(q_row, torch.float16, "q_row"), int(q_head),
-        int(tok_begin), int(tok_end), _ptr(dots, torch.int32, "dots"), _ptr(dev_status, torch.int32, "dev_status"),
-        _stream(stream)))
+        ctypes.byref(shape), ctypes.byref(lc), arr, _ptr(q, torch.float16, "q"), _ptr(parent, torch.int32, "parent"),
+        int(t_nodes), _ptr(workspace, name="workspace"), workspace.numel() * workspace.element_size(),
+        _ptr(dots, torch.int32, "dots"), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
 
 
 def stv_verify_attn_no_alloc(shape, layer: LayerCache, seqs, q, parent, t_nodes: int, path, o, dev_status=None,

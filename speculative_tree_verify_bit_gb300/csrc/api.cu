@@ -179,7 +179,7 @@ const char* stv_status_string(int status) {
   }
 }
 
-int stv_version(void) { return 1; }
+int stv_version(void) { return 2; }
 
 int stv_page_bytes(const stv_shape* shape, int64_t* bytes) {
   int rc = check_shape(shape, -1, nullptr);
@@ -233,7 +233,8 @@ int stv_verify_workspace_bytes(const stv_shape* shape, const stv_seq* seqs, int 
 // stv_verify_attn, and stv_append_verify_attn when k_tree / v_tree are given.
 static int verify_common(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs, int n_seqs,
                          const void* k_tree, const void* v_tree, const void* q, const int32_t* parent, int t_nodes,
-                         int path, void* workspace, size_t ws_bytes, int32_t* dev_status, stv_stream_t stream) {
+                         int path, void* workspace, size_t ws_bytes, int32_t* dev_status, stv_stream_t stream,
+                         int32_t* dots = nullptr) {
   ShapeInfo sh;
   int rc = check_shape(shape, t_nodes, &sh);
   if (rc) return rc;
@@ -271,6 +272,7 @@ static int verify_common(const stv_shape* shape, const stv_layer_cache* layer, c
   p.k_tree = static_cast<const __half*>(k_tree);
   p.v_tree = static_cast<const __half*>(v_tree);
   p.i4 = sh.i4;
+  p.dots = dots;
   p.status = dev_status;
   cudaStream_t s = (cudaStream_t)stream;
   if (path == STV_PATH_INT8) {
@@ -419,30 +421,16 @@ int stv_kv_commit(const stv_shape* shape, const stv_layer_cache* layers, int n_l
   return to_status(launch_kv_commit(p, (cudaStream_t)stream));
 }
 
-int stv_int8_qk_dots(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seq, const void* q_row,
-                     int q_head, int32_t tok_begin, int32_t tok_end, int32_t* dots, int32_t* dev_status,
-                     stv_stream_t stream) {
+int stv_int8_qk_dots(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seq, const void* q,
+                     const int32_t* parent, int t_nodes, void* workspace, size_t ws_bytes, int32_t* dots,
+                     int32_t* dev_status, stv_stream_t stream) {
   ShapeInfo sh;
-  int rc = check_shape(shape, -1, &sh);
+  int rc = check_shape(shape, t_nodes, &sh);
   if (rc) return rc;
-  if ((rc = check_layer(layer, sh)) || (rc = check_seqs(seq, 1, 0))) return rc;
-  if (sh.i4) return STV_ERR_UNIMPLEMENTED;  // the inspection reads the 3-bit groups
-  if (!q_row || !dots || q_head < 0 || q_head >= sh.hq) return STV_ERR_INVALID_ARG;
-  if (tok_begin < 0 || tok_end < tok_begin || (int64_t)tok_end > (int64_t)seq->n_pages * kPageTok)
-    return STV_ERR_INVALID_ARG;
-  VerifyParams p;
-  memset(&p, 0, sizeof(p));
-  fill_seq_descs(p.seq, seq, 1, nullptr);
-  p.n_seqs = 1;
-  p.hq = sh.hq;
-  p.hkv = sh.hkv;
-  p.G = sh.G;
-  p.pool = layer->pool;
-  p.page_bytes = layer->page_bytes;
-  p.pool_pages = layer->n_pages;
-  p.status = dev_status;
-  return to_status(launch_int8_dots(p, 0, static_cast<const __half*>(q_row), q_head, tok_begin, tok_end, dots,
-                                    (cudaStream_t)stream));
+  if (sh.i4) return STV_ERR_UNIMPLEMENTED;  // the per-group dots belong to the 3-bit cache
+  if (!dots) return STV_ERR_INVALID_ARG;
+  return verify_common(shape, layer, seq, 1, nullptr, nullptr, q, parent, t_nodes, STV_PATH_INT8, workspace, ws_bytes,
+                       dev_status, stream, dots);
 }
 
 }  // extern "C"

@@ -96,6 +96,9 @@ struct VerifyParams {
   const __half* k_tree;
   const __half* v_tree;
   int i4;  // int4 per-token-head cache
+  // Inspection (int8 path, one sequence): when set, the verify kernel also
+  // writes its own per-group integer dots, int32 [hkv][R][ctx + T][8].
+  int32_t* dots;
   int32_t* status;
 };
 
@@ -147,11 +150,10 @@ cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_chain_parents(int32_t* parent, int chunks, int t, cudaStream_t s);
 cudaError_t launch_kv_commit(const CommitParams& p, cudaStream_t s);
 cudaError_t launch_quantize_q(const __half* q, int n_rows, int8_t* qi, float* sq, cudaStream_t s);
-cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);
+cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);     // exact path; int4 cache (verify_tc.cu)
+cudaError_t launch_verify_i8(const VerifyParams& p, cudaStream_t s);  // int8 path, 3-bit cache (verify_i8.cu)
 cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_tree_accept(const int32_t* parent, const int32_t* draft, const int32_t* argmax, int T, int n_seqs,
                                int32_t* n_commit, int32_t* path, int32_t* out_ids, int32_t* status, cudaStream_t s);
-cudaError_t launch_int8_dots(const VerifyParams& p, int seq, const __half* q_row, int q_head, int tok_begin,
-                             int tok_end, int32_t* dots, cudaStream_t s);
 
 }  // namespace stv

@@ -1,13 +1,9 @@
 // verify_aux.cu -- the kernels around the tensor-core verify kernel: the int8
-// Q quantizer (a3), split_combine (a5) and the int8-dots inspection kernel.
+// Q quantizer (a3), split_combine (a5) and the prefill chain parents.
 //
 // Sources: "elpis" README, "Why fast" (8-row token tree verified in one pass;
 // decode verify with 3-bit K codes as exact int8 against int8 Q); Reddit
 // posts (u/iamMess), second post (split-KV verify attention).
-//
-// The int8-dots kernel decodes K with the same block decoder as the verify
-// kernel and accumulates the per-group products of qi and (code - 4) as
-// integers, so its output can be compared bit for bit.
 #include "stv_device.cuh"
 
 namespace stv {
@@ -119,47 +115,6 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const __grid_constan
 cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t s) {
   const int warps = p.n_seqs * p.hkv * p.R * 4;  // four channel quarters per row
   split_combine_kernel<<<(warps + 7) / 8, 256, 0, s>>>(p);
-  return cudaGetLastError();
-}
-
-// ---------------------------------------------------------------------------
-// Inspection: exact int8 per-group dots of one Q row against a key range.
-
-__global__ void __launch_bounds__(256) int8_dots_kernel(const __grid_constant__ VerifyParams p, int s,
-                                                        const __half* __restrict__ q_row, int q_head, int tok_begin,
-                                                        int tok_end, int32_t* __restrict__ dots) {
-  __shared__ __align__(16) int8_t qi[kHeadDim];
-  __shared__ float sq;
-  if (threadIdx.x < 32) quantize_q_row_warp(q_row, qi, &sq);
-  __syncthreads();
-  const int h = q_head / p.G;
-  const int n = tok_end - tok_begin;
-  for (int idx = blockIdx.x * 256 + threadIdx.x; idx < n * kGroups; idx += gridDim.x * 256) {
-    const int j = idx / kGroups, g = idx % kGroups, tok = tok_begin + j;
-    const uint8_t* hb = head_block(p.seq[s], p.pool, p.page_bytes, p.pool_pages, tok, h, p.status);
-    int acc = 0;
-    if (hb) {
-      const int slot = tok & (kPageTok - 1);
-      const uint32_t* wp = reinterpret_cast<const uint32_t*>(hb + kOffKCodes + slot * 96 + g * 12);
-      __half2 out[16];
-      decode_block_raw(wp[0], wp[1], wp[2], out);
-#pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        float2 f = __half22float2(out[m]);
-        acc += (int)qi[g * kGroup + 2 * m] * (int)f.x + (int)qi[g * kGroup + 2 * m + 1] * (int)f.y;
-      }
-    }
-    dots[idx] = acc;
-  }
-}
-
-cudaError_t launch_int8_dots(const VerifyParams& p, int seq, const __half* q_row, int q_head, int tok_begin,
-                             int tok_end, int32_t* dots, cudaStream_t s) {
-  const int n = (tok_end - tok_begin) * kGroups;
-  if (n <= 0) return cudaSuccess;
-  int blocks = (n + 255) / 256;
-  if (blocks > 1024) blocks = 1024;
-  int8_dots_kernel<<<blocks, 256, 0, s>>>(p, seq, q_row, q_head, tok_begin, tok_end, dots);
   return cudaGetLastError();
 }
 

@@ -25,14 +25,18 @@
 // operands, 128-byte swizzled K-major; K double-buffered, V^T triple-buffered
 // (the unpack may store V of tile i while P.V reads tiles i-1 and i-2, which
 // measured 4.6 % faster at 262K than two buffers); the raw ring.
-// Both paths use the fp16 tensor pipe (sm_103a has no kind::i8): the int8
-// path feeds qi (integers, exact in fp16) and scales the scores by sQ.
+// This kernel runs the exact path on the 3-bit cache and both paths on the
+// int4 cache (one K scale per key: Q.K over the exact codes, then the score
+// times the key's scale, so the int8 path's integer dot is formed exactly in
+// the fp32 accumulator).  The int8 path on the 3-bit cache, whose definition
+// needs per-group integer dots, runs in verify_i8.cu.
 // Softmax is online in fp32 with a stale-maximum threshold: P uses a
 // reference maximum that is raised (rescaling O and l) only when a score
 // exceeds it by more than 2^8, so P <= 256 in fp16 and O rescales are rare.
 // Every wait is bounded; a timeout sets a CTA abort flag, every role stops,
 // in-flight copies and MMAs are waited for (bounded) and TMEM is freed.
 #include "stv_device.cuh"
+#include "tc_util.cuh"
 
 namespace stv {
 namespace {
@@ -75,18 +79,10 @@ struct Fmt<true> {
 };
 static_assert(Fmt<true>::stages <= kStages, "barrier arrays");
 static_assert(Fmt<true>::smem <= 232448, "shared memory per CTA");
-constexpr uint32_t kWaitLimit = 1u << 20;   // try_wait calls before a wait gives up
-constexpr uint32_t kSuspendHintNs = 20000;  // per try_wait
-constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 
 constexpr uint32_t kColQ = 0, kColS0 = 128, kColO = 256, kTmemCols = 512;
 
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
-  return (1u << 4)                     // D: f32
-         | ((uint32_t)(N >> 3) << 17)  // N
-         | ((uint32_t)(M >> 4) << 24);  // M; A, B f16 K-major
-}
 constexpr uint32_t kIdescQK = idesc_f16_f32(128, 64);
 constexpr uint32_t kIdescPV = idesc_f16_f32(128, 256);
 
@@ -103,143 +99,16 @@ struct Bars {
 
 static_assert(sizeof(Bars) <= 1024, "barrier block");
 
-__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
-
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t n) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
-}
-// try_wait suspends the thread (up to the hint, in ns) until the phase
-// completes, so a waiting warp does not take issue slots from working ones.
-__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(su32(b)), "r"(parity), "r"(kSuspendHintNs)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait by one thread.  False on timeout or when the CTA aborted.
+// Waits suspend (try_wait with a time hint): measured faster here than
+// polling, since this kernel's roles mostly wait on the tensor pipe.
 __device__ __forceinline__ bool wait1(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
-    if (mbar_try(b, parity)) return true;
-    if ((it & 63) == 63 && *abort_flag) return false;
-  }
-  *abort_flag = 1;
-  return false;
+  return stv::wait1<false>(b, parity, abort_flag);
 }
-// Non-blocking check of a phase.  Even a completed phase costs a waiting
-// warp a shared-memory round trip (a few hundred cycles under load), so a
-// warp that needs several barriers checks them all at once, letting the
-// round trips overlap, and then settles each one: `settle` blocks only if
-// some lane saw that phase incomplete.  A phase seen complete stays so until
-// the warp's own next arrival, so an early check remains valid.
-__device__ __forceinline__ uint32_t probe(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile("{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-               : "=r"(ok) : "r"(su32(b)), "r"(parity) : "memory");
-  return ok;
-}
-// Bounded wait by a whole warp; the result is warp-uniform.
 __device__ __forceinline__ bool waitw(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
-  bool ok = wait1(b, parity, abort_flag);
-  return __all_sync(0xffffffffu, ok);
+  return stv::waitw<false>(b, parity, abort_flag);
 }
-// Completes a `probe`: true at once when every lane saw the phase complete.
 __device__ __forceinline__ bool settle(uint64_t* b, uint32_t parity, uint32_t probed, volatile int* abort_flag) {
-  if (__all_sync(0xffffffffu, probed)) return true;
-  return waitw(b, parity, abort_flag);
-}
-
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   su32(dst)),
-               "l"(src), "r"(bytes), "r"(su32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, __half2 a, __half2 b, __half2 c, __half2 d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(h2u(a)), "r"(h2u(b)), "r"(h2u(c)), "r"(h2u(d))
-               : "memory");
-}
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-// Issued by one elected lane of a converged warp: the warp runs the MMA loop
-// in uniform control flow, so descriptors stay in uniform registers.
-__device__ __forceinline__ void tc_commit(uint64_t* b) {
-  asm volatile(
-      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
-      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(su32(b))
-      : "memory");
-}
-__device__ __forceinline__ void mma_tmemA(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p, e;\n setp.ne.u32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
-      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
-      "r"(a), "l"(bdesc), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
-#define STV_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
-#define STV_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
-
-// 32 consecutive 32-bit columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%"
-      "19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : STV_R8(0), STV_R8(8), STV_R8(16), STV_R8(24)
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      STV_W8(0), STV_W8(8), STV_W8(16), STV_W8(24)
-      : "memory");
-}
-// Wait for this thread's TMEM loads; the registers are ordered after the wait.
-__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
-}
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// Shared-memory matrix descriptor: 128-byte swizzle, K-major, 8-row groups
-// 1024 bytes apart (stride byte offset), sm_100-family version field.
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// 128-byte-swizzled K-major tile: rows of 128 bytes in 8-row groups of 1024
-// bytes; 16-byte chunk c of row `row` sits at chunk c ^ (row % 8).  A row's
-// base with its XOR term folded in makes each chunk address one XOR.
-__device__ __forceinline__ uint32_t sw128_row(int row) {
-  return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((row & 7) << 4));
-}
-__device__ __forceinline__ uint32_t sw128_chunk(uint32_t row_base, int c) { return row_base ^ (uint32_t)(c << 4); }
-
-// 2^x with the SFU's approximate exponential (inputs here are <= 8; results
-// below the normal range flush to zero, which a softmax weight can afford).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
+  return stv::settle<false>(b, parity, probed, abort_flag);
 }
 
 // kAppend: the round's tree rows are packed into the cache by this launch
@@ -821,6 +690,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
 }  // namespace
 
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s) {
+  // the int8 path on the 3-bit cache forms per-group integer dots: its own kernel
+  if (p.path == STV_PATH_INT8 && !p.i4) return launch_verify_i8(p, s);
   const bool append = p.k_tree != nullptr && p.v_tree != nullptr;
   // the fused append packs the 3-bit cache only (the host refuses it for int4)
   auto kernel = p.i4 ? verify_tc_kernel<false, true>

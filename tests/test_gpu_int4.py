@@ -137,7 +137,7 @@ def test_unimplemented_entry_points(gpu):
         stv.stv_append_verify_attn(r.shape, r.layer, r.seqs, kt, kt, r.q, torch.as_tensor(r.parent, device=gpu), 4,
                                    "exact", ws)
     assert e.value.status == stv.STV_ERR_UNIMPLEMENTED
-    dots = torch.zeros((8, 8), dtype=torch.int32, device=gpu)
+    dots = torch.zeros((4, 4 * 6, 104, 8), dtype=torch.int32, device=gpu)
     with pytest.raises(stv.StvError) as e:
-        stv.stv_int8_qk_dots(r.shape, r.layer, r.seqs[0], r.q[0, 0, 0].contiguous(), 0, 0, 8, dots)
+        stv.stv_int8_qk_dots(r.shape, r.layer, r.seqs[0], r.q, torch.as_tensor(r.parent, device=gpu), 4, ws, dots)
     assert e.value.status == stv.STV_ERR_UNIMPLEMENTED

@@ -116,18 +116,35 @@ def test_full_size_other_layers(gpu, name, layers):
         del r
 
 
-def test_int8_dots_bit_exact(gpu):
-    r = Round([700], 16, seed=77)
+@pytest.mark.parametrize("ctx,t,hq,hkv", [
+    ([700], 16, 24, 4),    # 716 keys: ragged last tile, one split per head
+    ([3000], 5, 24, 4),    # several splits per head, 30 rows
+    ([511], 32, 16, 4),    # 128 rows per KV head: one group per QK round
+])
+def test_int8_dots_bit_exact(gpu, ctx, t, hq, hkv):
+    """The int8 path's per-group integer dots I_g, as the verify kernel forms
+    them on the tensor cores (every row, every key of [0, ctx + T), every
+    group), equal the oracle's exact integers bit for bit; the same launch's
+    attention output stays within the tolerance."""
+    r = Round(ctx, t, seed=77 + t, hq=hq, hkv=hkv)
     layer = r.gpu_cache()
     r.oracle_cache()
+    G, n = hq // hkv, ctx[0] + t
+    ws = torch.empty(stv.stv_verify_workspace_bytes(r.shape, r.seqs, t), dtype=torch.uint8, device=gpu)
+    dots = torch.full((hkv, t * G, n, 8), -(2 ** 31), dtype=torch.int32, device=gpu)
+    parent = torch.as_tensor(r.parent, device=gpu)
+    stv.stv_int8_qk_dots(r.shape, layer, r.seqs[0], r.q, parent, t, ws, dots)
+    o = torch.empty((1, t, hq, 256), dtype=torch.float16, device=gpu)
+    stv.stv_split_combine(r.shape, r.seqs, t, ws, o)
+    torch.cuda.synchronize()
+    got = dots.cpu().numpy()
     qn = r.q.cpu().numpy()
-    for node, qh in ((0, 0), (5, 11), (15, 23)):
-        q_row = r.q[0, node, qh].contiguous()
-        dots = torch.zeros((716, 8), dtype=torch.int32, device=gpu)
-        stv.stv_int8_qk_dots(r.shape, layer, r.seqs[0], q_row, qh, 0, 716, dots)
-        torch.cuda.synchronize()
-        want = oracle.int8_dots(r.ocache, r.tables, 0, qn[0, node, qh], qh, r.hq, 0, 716)
-        assert np.array_equal(dots.cpu().numpy(), want)
+    for h in range(hkv):
+        for row in range(t * G):
+            node, qh = row // G, h * G + row % G
+            want = oracle.int8_dots(r.ocache, r.tables, 0, qn[0, node, qh], qh, r.hq, 0, n)
+            assert np.array_equal(got[h, row], want), f"KV head {h} row {row}"
+    assert_attention_close(o.float().cpu().numpy(), r.oracle_attention("int8"), f"{ctx}/{t}/int8 (dump launch)")
 
 
 def test_deterministic_run_to_run(gpu):
