@@ -65,6 +65,19 @@ def verify_kernel_bytes(ctx_list, t, hq=24, hkv=4, kv_format="bit3"):
     return sum(c + t for c in ctx_list) * hkv * KV_FORMATS[kv_format][1] + len(ctx_list) * t * hq * 256 * 2
 
 
+def verify_kernel_flops(ctx_list, t, hq=24):
+    """Algorithmic FLOPs of one verify launch: Q.K^T and P.V over every
+    visible key, 2 x 2 x hq x 256 per (node, key) (the tree mask's hidden
+    keys counted, as the MMA tile computes them)."""
+    return sum(c + t for c in ctx_list) * t * hq * 256 * 4
+
+
+def launches_per_step(args, w: workloads.Workload) -> int:
+    L = args.layers or w.layers
+    per_layer = (2 if args.fuse_append else 3) + (1 if args.path == "int8" else 0)
+    return L * per_layer + 2
+
+
 def measured_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -234,9 +247,16 @@ class GpuRound:
         self.out_ids = torch.zeros((n, T), dtype=torch.int32, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
 
-    def launches_per_step(self, path):
-        per_layer = (2 if self.fuse_append else 3) + (1 if path == "int8" else 0)
-        return self.L * per_layer + 2
+    def set_trees(self, p_accept: float):
+        """Draw the round's trees for another acceptance probability into the
+        same device buffers (a captured graph keeps reading them)."""
+        import torch
+
+        rt = workloads.round_trees(self.w, p_accept)
+        self.parent.copy_(torch.as_tensor(rt.parent))
+        self.draft.copy_(torch.as_tensor(rt.draft))
+        self.argmax.copy_(torch.as_tensor(rt.argmax))
+        torch.cuda.synchronize()
 
     def step(self, path, verify_events=None):
         stv = self.stv
@@ -414,6 +434,84 @@ def us_per_layer_round(round_ms: float, layers: int, world: int) -> float:
     return round_ms * 1e3 / (layers * world)
 
 
+def graph_event():
+    """An event record node inside a CUDA graph (timing-capable), if this
+    PyTorch can make one."""
+    import torch
+
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        return None
+
+
+def time_round(r: GpuRound, path: str, steps: int, warmup: int, barrier, dev):
+    """The round (L x append/verify/combine, accept, commit) captured once in
+    a CUDA graph, with event record nodes around each layer's verify launch;
+    `steps` replays timed with CUDA events, clocks sampled meanwhile.
+    Returns the replay times (ms), the verify launch times (ms) and the clock
+    summary."""
+    import torch
+
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(warmup):
+            r.step(path)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    ev = [[graph_event(), graph_event()] for _ in range(r.L)]
+    if any(e is None for pair in ev for e in pair):
+        ev = None
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        r.step(path, verify_events=ev)
+    for _ in range(warmup):
+        graph.replay()
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    barrier()
+    with ClockSampler(dev.index) as clk:
+        marks[0].record()
+        for k in range(steps):
+            graph.replay()
+            marks[k + 1].record()
+        barrier()
+    round_ms = [marks[k].elapsed_time(marks[k + 1]) for k in range(steps)]
+    # per-launch verify time: the event nodes of a few more replays
+    verify_ms = []
+    for _ in range(5):
+        if ev is not None:
+            graph.replay()
+            torch.cuda.synchronize()
+            verify_ms += [a.elapsed_time(b) for a, b in ev]
+        else:  # no event nodes: the same launches, eagerly, with events around verify
+            ev_eager = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(r.L)]
+            r.step(path, verify_events=ev_eager)
+            torch.cuda.synchronize()
+            verify_ms += [a.elapsed_time(b) for a, b in ev_eager]
+    del graph
+    return round_ms, verify_ms, clk.summary()
+
+
+def config_line(w: workloads.Workload, path: str, p_accept: float, kv_format: str, round_ms, verify_ms, clocks,
+                layers: int, status: int) -> dict:
+    """One workload's figures: round time per layer-round, the verify
+    launch, its algorithmic bytes and FLOPs and their fractions of the
+    measured HBM and dense fp16/bf16 tensor peaks."""
+    us_lr = statistics.median(round_ms) * 1e3 / layers
+    v_us = statistics.mean(verify_ms) * 1e3
+    vbytes = verify_kernel_bytes(w.ctx, w.t_nodes, w.hq, w.hkv, kv_format)
+    vflops = verify_kernel_flops(w.ctx, w.t_nodes, w.hq)
+    hbm, _ = measured_peak()
+    tf, _ = measured_bf16_peak()
+    gbs = vbytes / (v_us * 1e-6) / 1e9
+    tflops = vflops / (v_us * 1e-6) / 1e12
+    return {"workload": w.name, "ctx": list(w.ctx), "path": path, "p_accept": p_accept, "kv_format": kv_format,
+            "us_per_layer_round": us_lr, "verify_us_per_launch": v_us, "algorithmic_bytes_per_launch": vbytes,
+            "algorithmic_flops_per_launch": vflops, "hbm_gbs": gbs, "hbm_frac": gbs / hbm, "tflops": tflops,
+            "tensor_frac": tflops / tf, "clocks": clocks, "dev_status": status}
+
+
 def run_gpu(args, rank, world):
     import torch
 
@@ -432,52 +530,7 @@ def run_gpu(args, rank, world):
             dist.barrier()
         torch.cuda.synchronize()
 
-    # The round (16 x append/verify/combine, accept, commit) is captured once
-    # in a CUDA graph, with event nodes around each layer's verify launch.
-    side = torch.cuda.Stream(device=dev)
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
-        for _ in range(args.warmup):
-            r.step(args.path)
-    torch.cuda.current_stream().wait_stream(side)
-    torch.cuda.synchronize()
-    def graph_event():
-        # an event record node inside the graph (timing-capable), if this
-        # PyTorch can make one
-        try:
-            return torch.cuda.Event(enable_timing=True, external=True)
-        except TypeError:
-            return None
-
-    ev = [[graph_event(), graph_event()] for _ in range(r.L)]
-    if any(e is None for pair in ev for e in pair):
-        ev = None
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        r.step(args.path, verify_events=ev)
-    for _ in range(args.warmup):
-        graph.replay()
-    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    barrier()
-    with ClockSampler(dev.index) as clk:
-        marks[0].record()
-        for k in range(args.steps):
-            graph.replay()
-            marks[k + 1].record()
-        barrier()
-    round_ms = [marks[k].elapsed_time(marks[k + 1]) for k in range(args.steps)]
-    total_ms = marks[0].elapsed_time(marks[-1])
-    # per-launch verify time: the event nodes of a few more replays
-    verify_ms = []
-    for _ in range(5):
-        if ev is not None:
-            graph.replay()
-            torch.cuda.synchronize()
-        else:  # no event nodes: the same launches, eagerly, with events around verify
-            ev_eager = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(r.L)]
-            r.step(args.path, verify_events=ev_eager)
-            torch.cuda.synchronize()
-        verify_ms += [a.elapsed_time(b) for a, b in (ev if ev is not None else ev_eager)]
+    round_ms, verify_ms, clocks = time_round(r, args.path, args.steps, args.warmup, barrier, dev)
     st = int(r.status.item())
 
     # e2e: host buffers, copies inside the timed region
@@ -504,41 +557,91 @@ def run_gpu(args, rank, world):
 
     med_ms = statistics.median(round_ms)  # a round = one graph replay
     extra = rank == 0 and not args.no_next_rows
+    configs = {}
+    if extra and args.workload == "long262k" and args.kv_format == "bit3" and not args.fuse_append:
+        # The rest of the metric: the other path and acceptance probabilities
+        # on the same resident 262K cache, then the 32K and ragged workloads.
+        # Fewer replays each: these are reported beside the headline.
+        n = max(5, min(args.steps, 20))
+        other = "int8" if args.path == "exact" else "exact"
+        rm, vm, ck = time_round(r, other, n, 3, barrier, dev)
+        configs[f"long262k/{other}/p{p_accept:g}"] = config_line(w, other, p_accept, "bit3", rm, vm, ck, r.L,
+                                                                  int(r.status.item()))
+        for pa in w.p_accept:
+            if pa == p_accept:
+                continue
+            r.set_trees(pa)
+            rm, vm, ck = time_round(r, args.path, n, 3, barrier, dev)
+            configs[f"long262k/{args.path}/p{pa:g}"] = config_line(w, args.path, pa, "bit3", rm, vm, ck, r.L,
+                                                                   int(r.status.item()))
+        r.set_trees(p_accept)
     lookup = measure_lookup(w, dev) if extra else None
     prefill = measure_prefill(dev) if extra else None
     int4 = measure_int4(w, p_accept, dev, args.path) if extra and args.kv_format == "bit3" else None
+    if configs:
+        del r
+        torch.cuda.empty_cache()
+        for name in ("tree32k", "ragged"):
+            w2 = workloads.WORKLOADS[name]
+            pa2 = w2.p_accept[0]
+            r2 = GpuRound(w2, pa2, dev)
+            rm, vm, ck = time_round(r2, args.path, n, 3, barrier, dev)
+            configs[f"{name}/{args.path}/p{pa2:g}"] = config_line(w2, args.path, pa2, "bit3", rm, vm, ck, r2.L,
+                                                                  int(r2.status.item()))
+            del r2
+            torch.cuda.empty_cache()
     med_ms, e2e_ms = max_over_ranks([med_ms, e2e_ms], dist, dev)
-    layer_rounds = args.steps * r.L * world
-    us_per_lr = us_per_layer_round(med_ms, r.L, world)
+    L = args.layers or w.layers
+    layer_rounds = args.steps * L * world
+    us_per_lr = us_per_layer_round(med_ms, L, world)
     e2e_us = e2e_ms * 1e3 / layer_rounds
     bytes_lr = algorithmic_bytes_per_layer_round(w.ctx, w.t_nodes, w.hq, w.hkv, args.kv_format)
     vbytes = verify_kernel_bytes(w.ctx, w.t_nodes, w.hq, w.hkv, args.kv_format)
+    vflops = verify_kernel_flops(w.ctx, w.t_nodes, w.hq)
     v_us = statistics.mean(verify_ms) * 1e3
     peak, peak_kind = measured_peak()
     achieved = vbytes / (v_us * 1e-6) / 1e9
     traffic = load_traffic(args.workload, args.path, args.kv_format)
     return dict(rank=rank, us_per_lr=us_per_lr, e2e_us=e2e_us, bytes_lr=bytes_lr, v_us=v_us, vbytes=vbytes,
-                peak=peak, peak_kind=peak_kind, achieved=achieved, clocks=clk.summary(), status=st, h2d=h2d,
-                d2h=d2h, launches=r.launches_per_step(args.path) * args.steps, p_accept=p_accept, traffic=traffic,
-                n_units=None, ws_bytes=r.ws_bytes, round_gbs=bytes_lr / (us_per_lr * 1e-6) / 1e9 / world,
-                lookup=lookup, prefill=prefill, int4=int4)
+                vflops=vflops, peak=peak, peak_kind=peak_kind, achieved=achieved, clocks=clocks, status=st,
+                h2d=h2d, d2h=d2h, launches=launches_per_step(args, w) * args.steps, p_accept=p_accept,
+                traffic=traffic, round_gbs=bytes_lr / (us_per_lr * 1e-6) / 1e9 / world, lookup=lookup,
+                prefill=prefill, int4=int4, configs=configs)
+
+
+KERNEL_SOURCES = {  # the files a verify launch's code comes from, per path and cache format
+    "verify_tc": ("csrc/verify_tc.cu", "csrc/tc_util.cuh", "csrc/stv_device.cuh"),
+    "verify_i8": ("csrc/verify_i8.cu", "csrc/tc_util.cuh", "csrc/stv_device.cuh"),
+}
+
+
+def verify_kernel_name(path: str, kv_format: str) -> str:
+    return "verify_i8" if path == "int8" and kv_format == "bit3" else "verify_tc"
+
+
+def kernel_sources_sha256(kernel: str) -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(ROOT, "speculative_tree_verify_bit_gb300", f), "rb").read())
+    return h.hexdigest()
 
 
 def load_traffic(workload, path, kv_format="bit3"):
     """DRAM bytes per verify launch from the committed ncu summary, or None
-    when there is none for this workload or the verify kernel's source has
-    changed since the counters were taken."""
-    import hashlib
-
+    when there is none for this workload or the kernel's sources have changed
+    since the counters were taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
         d = json.load(open(p))
-        src = os.path.join(ROOT, "speculative_tree_verify_bit_gb300", "csrc", "verify_tc.cu")
-        if d.get("verify_tc_sha256") != hashlib.sha256(open(src, "rb").read()).hexdigest():
+        key = f"{workload}/{path}" + ("" if kv_format == "bit3" else f"/{kv_format}")
+        e = d.get("launches", {}).get(key)
+        if not e or e.get("sources_sha256") != kernel_sources_sha256(verify_kernel_name(path, kv_format)):
             return None
-        return d.get(f"{workload}/{path}" + ("" if kv_format == "bit3" else f"/{kv_format}"))
+        return e.get("dram_bytes")
     except Exception:
         return None
 
@@ -666,8 +769,11 @@ def main():
     if not args.no_cpu_baseline and world == 1:
         threads = os.cpu_count() or 1
         v, dt, sample = oracle_sample(w, args.oracle_rows, threads, args.kv_format)
-        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
-    frac = res["achieved"] / res["peak"]
+        v1, dt1, sample1 = oracle_sample(w, max(1, args.oracle_rows // 8), 1, args.kv_format)
+        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
+               "value_1thread": v1, "sample_1thread": sample1}
+    tf_peak, tf_kind = measured_bf16_peak()
+    tflops = res["vflops"] / (res["v_us"] * 1e-6) / 1e12
     line = {
         "metric": METRIC, "value": res["us_per_lr"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["us_per_lr"] * (args.layers or w.layers) * world / 1e3, "higher_is_better": False,
@@ -676,15 +782,23 @@ def main():
         "gbs_per_layer_round": res["round_gbs"],
         "bytes_per_layer_round": res["bytes_lr"],
         "verify_us_per_launch": res["v_us"],
-        "roofline": {"bound": "hbm", "achieved": res["achieved"], "peak": res["peak"], "unit": "GB/s",
-                     "frac": frac, "traffic": res["traffic"], "kernel": "verify_attn",
-                     "algorithmic_bytes_per_launch": res["vbytes"], "peak_source": res["peak_kind"]},
+        # The verify launch's arithmetic intensity (FLOPs per algorithmic byte)
+        # is above the GPU's ridge point, so its roofline is the dense fp16
+        # tensor peak; the HBM figures are beside it.
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": tf_peak, "unit": "TFLOP/s",
+                     "frac": tflops / tf_peak, "traffic": res["traffic"], "kernel": "verify_attn",
+                     "algorithmic_flops_per_launch": res["vflops"], "algorithmic_bytes_per_launch": res["vbytes"],
+                     "arithmetic_intensity": res["vflops"] / res["vbytes"], "ridge": tf_peak * 1e3 / res["peak"],
+                     "peak_source": f"{tf_kind} dense bf16 burst (fp16 runs at the same rate)",
+                     "hbm_achieved_gbs": res["achieved"], "hbm_peak_gbs": res["peak"],
+                     "hbm_frac": res["achieved"] / res["peak"], "hbm_peak_source": res["peak_kind"]},
         "cpu_baseline": cpu,
         "e2e": {"value": res["e2e_us"], "unit": UNIT, "h2d_bytes_per_step": res["h2d"],
                 "d2h_bytes_per_step": res["d2h"]},
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
         "dev_status": res["status"],
+        "configs": res["configs"],
         "next_rows": {"lookup_draft": res.get("lookup"), "prefill_attn": res.get("prefill"),
                       "int4_cache_verify": res.get("int4")},
     }

@@ -208,6 +208,20 @@ int stv_append_verify_attn(const stv_shape* shape, const stv_layer_cache* layer,
                            int path, void* workspace, size_t ws_bytes, int32_t* dev_status, stv_stream_t stream);
 
 /*
+ * Failure-path test of stv_verify_attn (the pages have no counterpart: it
+ * exists to test this library's failure detection without a GPU fault).
+ * Same arguments and checks as stv_verify_attn, but the kernel's producer
+ * issues none of its copies, so the waits on them never complete: every
+ * wait gives up after its bound (about 1.3 s), the kernel stops every role,
+ * waits for anything it issued, frees its tensor memory, ORs
+ * STV_DEV_TIMEOUT into *dev_status and returns.  The workspace's partials
+ * are then invalid; the CUDA context stays usable.
+ */
+int stv_verify_attn_timeout_test(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs,
+                                 int n_seqs, const void* q, const int32_t* parent, int t_nodes, int path,
+                                 void* workspace, size_t ws_bytes, int32_t* dev_status, stv_stream_t stream);
+
+/*
  * a5 -- merge the split partials of the last stv_verify_attn on this
  * workspace: per row M = max_s m_s, O = sum_s 2^(m_s - M) O_s / sum_s
  * 2^(m_s - M) l_s, splits taken in a fixed order (deterministic).
@@ -237,8 +251,11 @@ int stv_tree_accept(const int32_t* parent, const int32_t* draft_ids, const int32
  * a7 -- compact the accepted rows: for every layer, KV head and i <
  * n_commit[s], the packed row at slot ctx + path[i] moves to slot ctx + i
  * (all sources are read before any destination is written), then
- * ctx_dev[s] += n_commit[s].  Sequences whose n_commit is outside [1, T]
- * are left untouched (STV_DEV_BAD_COMMIT).
+ * ctx_dev[s] += n_commit[s].  A sequence is committed in every layer or in
+ * none: one whose n_commit is outside [1, T] or whose path is not a root
+ * path is left untouched (STV_DEV_BAD_COMMIT), and so is one whose source or
+ * destination positions are past its page table or map to a page outside
+ * any layer's pool (STV_DEV_BAD_PAGE); ctx_dev[s] then stays as it was.
  *  layers:   host array of n_layers caches (device pools).
  *  n_commit, path: device, as written by stv_tree_accept.
  *  ctx_dev:  device int32 [n_seqs] (may be NULL).

@@ -45,7 +45,7 @@ EXPORTS = (
     "stv_status_string", "stv_version", "stv_page_bytes", "stv_kv_append_pack", "stv_verify_workspace_bytes",
     "stv_verify_attn", "stv_split_combine", "stv_tree_accept", "stv_kv_commit", "stv_int8_qk_dots",
     "stv_verify_attn_no_alloc", "stv_append_verify_attn", "stv_lookup_workspace_bytes", "stv_lookup_draft",
-    "stv_prefill_workspace_bytes", "stv_prefill_attn",
+    "stv_prefill_workspace_bytes", "stv_prefill_attn", "stv_verify_attn_timeout_test",
 )
 
 
@@ -115,6 +115,8 @@ def load() -> ctypes.CDLL:
         lib.stv_append_verify_attn.argtypes = [P, P, P, I, P, P, P, P, I, I, P, ctypes.c_size_t, P, P]
         lib.stv_verify_attn_no_alloc.restype = I
         lib.stv_verify_attn_no_alloc.argtypes = [P, P, P, I, P, P, I, I, P, P, P]
+        lib.stv_verify_attn_timeout_test.restype = I
+        lib.stv_verify_attn_timeout_test.argtypes = [P, P, P, I, P, P, I, I, P, ctypes.c_size_t, P, P]
         _lib = lib
     return _lib
 
@@ -315,6 +317,21 @@ def stv_int8_qk_dots(shape, layer: LayerCache, seq: Seq, q, parent, t_nodes: int
         ctypes.byref(shape), ctypes.byref(lc), arr, _ptr(q, torch.float16, "q"), _ptr(parent, torch.int32, "parent"),
         int(t_nodes), _ptr(workspace, name="workspace"), workspace.numel() * workspace.element_size(),
         _ptr(dots, torch.int32, "dots"), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+
+
+def stv_verify_attn_timeout_test(shape, layer: LayerCache, seqs, q, parent, t_nodes: int, path, workspace,
+                                 dev_status=None, stream=None):
+    """stv_verify_attn with the kernel's copies withheld: every wait runs out
+    and the kernel reports STV_DEV_TIMEOUT (failure-path test)."""
+    import torch
+
+    lc = layer.c()
+    arr = _seq_array(seqs)
+    path = PATHS.get(path, path)
+    _check("stv_verify_attn_timeout_test", load().stv_verify_attn_timeout_test(
+        ctypes.byref(shape), ctypes.byref(lc), arr, len(seqs), _ptr(q, torch.float16, "q"),
+        _ptr(parent, torch.int32, "parent"), int(t_nodes), int(path), _ptr(workspace, name="workspace"),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
 
 
 def stv_verify_attn_no_alloc(shape, layer: LayerCache, seqs, q, parent, t_nodes: int, path, o, dev_status=None,

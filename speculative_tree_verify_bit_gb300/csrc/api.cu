@@ -234,7 +234,7 @@ int stv_verify_workspace_bytes(const stv_shape* shape, const stv_seq* seqs, int 
 static int verify_common(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs, int n_seqs,
                          const void* k_tree, const void* v_tree, const void* q, const int32_t* parent, int t_nodes,
                          int path, void* workspace, size_t ws_bytes, int32_t* dev_status, stv_stream_t stream,
-                         int32_t* dots = nullptr) {
+                         int32_t* dots = nullptr, int withhold_copies = 0) {
   ShapeInfo sh;
   int rc = check_shape(shape, t_nodes, &sh);
   if (rc) return rc;
@@ -273,6 +273,7 @@ static int verify_common(const stv_shape* shape, const stv_layer_cache* layer, c
   p.v_tree = static_cast<const __half*>(v_tree);
   p.i4 = sh.i4;
   p.dots = dots;
+  p.test_withhold_copies = withhold_copies;
   p.status = dev_status;
   cudaStream_t s = (cudaStream_t)stream;
   if (path == STV_PATH_INT8) {
@@ -296,6 +297,13 @@ int stv_append_verify_attn(const stv_shape* shape, const stv_layer_cache* layer,
   if (!k_tree || !v_tree) return STV_ERR_INVALID_ARG;
   return verify_common(shape, layer, seqs, n_seqs, k_tree, v_tree, q, parent, t_nodes, path, workspace, ws_bytes,
                        dev_status, stream);
+}
+
+int stv_verify_attn_timeout_test(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs,
+                                 int n_seqs, const void* q, const int32_t* parent, int t_nodes, int path,
+                                 void* workspace, size_t ws_bytes, int32_t* dev_status, stv_stream_t stream) {
+  return verify_common(shape, layer, seqs, n_seqs, nullptr, nullptr, q, parent, t_nodes, path, workspace, ws_bytes,
+                       dev_status, stream, nullptr, 1);
 }
 
 int stv_split_combine(const stv_shape* shape, const stv_seq* seqs, int n_seqs, int t_nodes, const void* workspace,
@@ -402,10 +410,12 @@ int stv_kv_commit(const stv_shape* shape, const stv_layer_cache* layers, int n_l
   if ((rc = check_seqs(seqs, n_seqs, t_nodes))) return rc;
   CommitParams p;
   memset(&p, 0, sizeof(p));
+  p.min_pool_pages = layers[0].n_pages;
   for (int l = 0; l < n_layers; ++l) {
     if ((rc = check_layer(&layers[l], sh))) return rc;
     p.pools[l] = layers[l].pool;
     p.pool_pages[l] = layers[l].n_pages;
+    p.min_pool_pages = std::min(p.min_pool_pages, layers[l].n_pages);
   }
   fill_seq_descs(p.seq, seqs, n_seqs, nullptr);
   p.n_seqs = n_seqs;

@@ -10,7 +10,9 @@
 // README, "Why fast": commit the longest matching path + 1).  One CTA per
 // (sequence, layer, KV head) reads every source row into shared memory before
 // writing any destination, because a destination slot can be the source slot
-// of a later row.
+// of a later row.  A sequence whose path or pages are bad is left untouched
+// in every layer (and its ctx_dev entry too): each CTA validates all of it
+// before writing anything.
 #include "stv_device.cuh"
 
 namespace stv {
@@ -97,6 +99,24 @@ cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t s) {
 
 // ---------------------------------------------------------------------------
 
+// Whether every page a sequence's commit touches (sources ctx + path[i] and
+// destinations ctx + i, i < n) is in its table and inside every layer's pool
+// (min_pool: the smallest pool).  Every CTA of the sequence (one per layer
+// and KV head) checks the same entries against the same bound, so they all
+// take the same decision: the commit is all or nothing.
+__device__ __forceinline__ bool commit_pages_ok(const SeqDesc& sd, const int* path_s, int n, int32_t min_pool) {
+  for (int i = 0; i < n; ++i) {
+    const int64_t pos[2] = {(int64_t)sd.ctx + path_s[i], (int64_t)sd.ctx + i};
+    for (int k = 0; k < 2; ++k) {
+      const int64_t lp = pos[k] >> 8;
+      if (lp >= sd.n_pages) return false;
+      const int32_t page = __ldg(sd.page_table + lp);
+      if (page < 0 || page >= min_pool) return false;
+    }
+  }
+  return true;
+}
+
 __global__ void __launch_bounds__(256) kv_commit_kernel(const __grid_constant__ CommitParams p) {
   int b = blockIdx.x;
   const int h = b % p.hkv;
@@ -123,11 +143,11 @@ __global__ void __launch_bounds__(256) kv_commit_kernel(const __grid_constant__ 
       prev = x;
     }
     n_s = n;
-    ok_s = ok;
+    ok_s = ok ? (commit_pages_ok(p.seq[s], path_s, n, p.min_pool_pages) ? 1 : 2) : 0;
   }
   __syncthreads();
-  if (!ok_s) {
-    if (leader) report(p.status, STV_DEV_BAD_COMMIT);
+  if (ok_s != 1) {
+    if (leader) report(p.status, ok_s == 0 ? STV_DEV_BAD_COMMIT : STV_DEV_BAD_PAGE);
     return;
   }
   const int n = n_s;
@@ -138,12 +158,7 @@ __global__ void __launch_bounds__(256) kv_commit_kernel(const __grid_constant__ 
   // Read every source row.
   for (int i = 0; i < n; ++i) {
     const int64_t src = (int64_t)sd.ctx + path_s[i];
-    const uint8_t* hb = head_block(sd, pool, p.page_bytes, pool_pages, src, h, tid == 0 ? p.status : nullptr);
-    if (!hb) {
-      // leave the rows alone: the sequence's table does not reach them
-      if (tid == 0) ok_s = 0;
-      continue;
-    }
+    const uint8_t* hb = head_block(sd, pool, p.page_bytes, pool_pages, src, h, nullptr);  // validated above
     const int slot = (int)(src & (kPageTok - 1));
     if (tid < 6)
       reinterpret_cast<uint4*>(krow[i])[tid] = reinterpret_cast<const uint4*>(hb + kOffKCodes + slot * 96)[tid];
@@ -162,7 +177,6 @@ __global__ void __launch_bounds__(256) kv_commit_kernel(const __grid_constant__ 
     }
   }
   __syncthreads();
-  if (!ok_s) return;
 
   // Write every destination row.
   for (int i = 0; i < n; ++i) {
@@ -222,11 +236,11 @@ __global__ void __launch_bounds__(256) kv_commit_i4_kernel(const __grid_constant
       prev = x;
     }
     n_s = n;
-    ok_s = ok;
+    ok_s = ok ? (commit_pages_ok(p.seq[s], path_s, n, p.min_pool_pages) ? 1 : 2) : 0;
   }
   __syncthreads();
-  if (!ok_s) {
-    if (leader) report(p.status, STV_DEV_BAD_COMMIT);
+  if (ok_s != 1) {
+    if (leader) report(p.status, ok_s == 0 ? STV_DEV_BAD_COMMIT : STV_DEV_BAD_PAGE);
     return;
   }
   const int n = n_s;
@@ -236,12 +250,7 @@ __global__ void __launch_bounds__(256) kv_commit_i4_kernel(const __grid_constant
 
   for (int i = 0; i < n; ++i) {
     const int64_t src = (int64_t)sd.ctx + path_s[i];
-    const uint8_t* hb =
-        head_block(sd, pool, p.page_bytes, pool_pages, src, h, tid == 0 ? p.status : nullptr, kI4HeadBytes);
-    if (!hb) {
-      if (tid == 0) ok_s = 0;
-      continue;
-    }
+    const uint8_t* hb = head_block(sd, pool, p.page_bytes, pool_pages, src, h, nullptr, kI4HeadBytes);  // validated
     const int slot = (int)(src & (kPageTok - 1)), tile = slot / kTileTok, within = slot % kTileTok;
     if (tid < 8)
       reinterpret_cast<uint4*>(krow[i])[tid] = reinterpret_cast<const uint4*>(hb + kI4OffKCodes + slot * 128)[tid];
@@ -254,7 +263,6 @@ __global__ void __launch_bounds__(256) kv_commit_i4_kernel(const __grid_constant
     vcode[i][tid] = (uint8_t)((w >> i4_pos(within & 7)) & 15u);
   }
   __syncthreads();
-  if (!ok_s) return;
 
   for (int i = 0; i < n; ++i) {
     const int64_t dst = (int64_t)sd.ctx + i;

@@ -99,6 +99,9 @@ struct VerifyParams {
   // Inspection (int8 path, one sequence): when set, the verify kernel also
   // writes its own per-group integer dots, int32 [hkv][R][ctx + T][8].
   int32_t* dots;
+  // Failure-path test (stv_verify_attn_timeout_test): the producer issues no
+  // copy, every wait on one runs out and the kernel reports STV_DEV_TIMEOUT.
+  int test_withhold_copies;
   int32_t* status;
 };
 
@@ -134,6 +137,7 @@ struct CommitParams {
   int n_seqs, n_layers, hkv, T;
   int64_t page_bytes;
   int32_t pool_pages[kMaxLayers];
+  int32_t min_pool_pages;  // the smallest of pool_pages
   const int32_t* n_commit;
   const int32_t* path;
   int32_t* ctx_dev;

@@ -13,7 +13,7 @@ namespace stv {
 namespace {
 
 constexpr uint32_t kSpinLimit = 1u << 13;   // test_wait polls before a polling wait starts suspending
-constexpr uint32_t kWaitLimit = 1u << 20;   // try_wait calls before a wait gives up
+constexpr uint32_t kWaitLimit = 1u << 16;   // try_wait calls before a wait gives up (about 1.3 s)
 constexpr uint32_t kSuspendHintNs = 20000;  // per try_wait
 constexpr float kLog2e = 1.4426950408889634f;
 

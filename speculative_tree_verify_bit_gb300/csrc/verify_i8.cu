@@ -28,15 +28,16 @@
 //               straight into tensor memory.
 //   warps 1-2   idle.
 // Per 64-key tile:
-//   I_g[128 rows x 64 keys] = Q_g (TMEM) . C_g^T (shared), one TMEM block of
-//                             64 columns per group, two groups per round
-//                             (one when T * G > 96), four (eight) rounds
+//   I_g[128 rows x 64 keys] = Q_g (TMEM) . C_g^T (shared), one group per
+//                             round (eight per tile), each round's dots in
+//                             one of two TMEM blocks of 64 columns (one
+//                             block when T * G > 96)
 //   O^T[256 ch x NP rows]  += V^T (TMEM, two 128-channel halves) . P^T (shared)
 // The second is P.V with the operands swapped (M = the 256 channels, N = the
 // NP = ceil16(T*G) real rows), which keeps the accumulator small enough to
 // leave room for the per-group dots.  Tensor memory (512 columns): qi as
-// fp16 [0,128); the round's dots [128, 128 + 64 * groups per round); one V^T
-// buffer of 64 columns; O^T halves of NO = ceil32(T*G) columns at the end.
+// fp16 [0,128); the rounds' dot blocks from column 128; one V^T buffer of
+// 64 columns; O^T halves of NO = ceil32(T*G) columns at the end.
 // Softmax is online in fp32 with a stale-maximum threshold: P uses a
 // reference maximum that is raised (rescaling O and l) only when a score
 // exceeds it by more than 2^8, so P <= 256 in fp16 and O rescales are rare.
@@ -73,7 +74,7 @@ struct Ctl {
   uint64_t kd_full[kKBuffers], kd_empty[kKBuffers];
   uint64_t vd_full, vd_empty;
   uint64_t ks_full[kSlots];
-  uint64_t s_full, s_free;
+  uint64_t s_full[2], s_free[2];
   uint64_t p_full[2], p_empty[2];
   uint64_t q_ready, mma_done;
   uint64_t tree_packed;  // the round's tree rows of this unit are in the cache (fused append)
@@ -110,8 +111,10 @@ __device__ __forceinline__ uint32_t softmax_bar_popc(bool pred) {
 }
 
 // kAppend: the round's tree rows are packed into the cache by this launch
-// (stv_append_verify_attn).
-template <bool kAppend>
+// (stv_append_verify_attn).  kWithhold (failure-path test only,
+// stv_verify_attn_timeout_test): the producer issues no copy, so every wait
+// on one runs out.
+template <bool kAppend, bool kWithhold = false>
 __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_constant__ VerifyParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment of the operand tiles (the swizzle works on address bits).
@@ -140,9 +143,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_con
   // ---- tensor-memory plan (R <= 128 rows) ----
   const int NP = (R + 15) & ~15;  // N of the P.V product
   const int NO = (R + 31) & ~31;  // columns of one O^T half
-  const int gpr = NO <= 96 ? 2 : 1;  // groups per QK round
-  const int rounds = kGroups / gpr;  // QK rounds per tile
-  const uint32_t s_end = kColS + 64 * gpr;  // the V^T buffer: [s_end, s_end + 64)
+  // One group per QK round (eight rounds per tile), its dots in one of nsb
+  // TMEM blocks of 64 columns: two (the MMA of round k + 1 overlaps the
+  // softmax warps' loads of round k) when the O^T halves leave room.
+  const int nsb = NO <= 96 ? 2 : 1;
+  const uint32_t s_end = kColS + 64 * nsb;  // the V^T buffer: [s_end, s_end + 64)
   const uint32_t colO = kTmemCols - 2 * NO;
 
   // ---- set-up ----
@@ -162,8 +167,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_con
       mbar_init(&ctl->p_full[i], 4);
       mbar_init(&ctl->p_empty[i], 1);
     }
-    mbar_init(&ctl->s_full, 1);
-    mbar_init(&ctl->s_free, 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->s_full[i], 1);
+      mbar_init(&ctl->s_free[i], 4);
+    }
     mbar_init(&ctl->q_ready, 4);
     mbar_init(&ctl->mma_done, 1);
     mbar_init(&ctl->tree_packed, 8);
@@ -202,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_con
     if (lane == 0) {
       int issued = 0;
       bool tree_ready = !kAppend;
-      for (int i = 0; i < n_tiles; ++i) {
+      for (int i = 0; i < (kWithhold ? 0 : n_tiles); ++i) {
         const int st = i % kStages;
         if (!wait1(&ctl->raw_empty[st], ((i / kStages) & 1) ^ 1, abort_flag)) break;
         const int key0 = tok0 + i * kTileTok;
@@ -238,8 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_con
   } else if (warp == 3) {
     // =================== MMA issuer (whole warp, one elected lane issues) ===================
     // Issue order: QK(0) (all rounds), then QK(i), PV(i-1) for i = 1, 2, ...,
-    // then PV(last).  Each QK round waits until the softmax warps have loaded
-    // the previous round's dots (one TMEM block per round).
+    // then PV(last).  A QK round reuses a TMEM block once the softmax warps
+    // have loaded the dots it held.
     // Descriptors are built once; each MMA then only adds a constant to the
     // start-address field (no carry: shared addresses are < 256 KiB).
     const uint32_t tm = tmem;
@@ -254,22 +261,21 @@ __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_con
                   abort_flag))
         return false;
       const uint64_t kd = kdesc0 + (uint64_t)(kb * (kOperandBytes >> 4));
-      for (int k = 0; k < rounds; ++k) {
-        if (rnd > 0 && !settle(&ctl->s_free, (rnd - 1) & 1, probe(&ctl->s_free, (rnd - 1) & 1), abort_flag))
+      for (int g = 0; g < kGroups; ++g) {
+        const int b = rnd % nsb;
+        const uint32_t u = rnd / nsb;  // this block's use count
+        if (u > 0 && !settle(&ctl->s_free[b], (u - 1) & 1, probe(&ctl->s_free[b], (u - 1) & 1), abort_flag))
           return false;
         tc_after();
-        // group g's 32 channels are K16 steps 2g and 2g + 1, into the round's
-        // 64 columns for that group
-        for (int gg = 0; gg < gpr; ++gg) {
+        // group g's 32 channels are K16 steps 2g and 2g + 1
 #pragma unroll
-          for (int t2 = 0; t2 < 2; ++t2) {
-            const int kk = 2 * (k * gpr + gg) + t2;
-            mma_tmemA(tm + kColS + 64 * gg, tm + kColQ + 8 * kk, kd + (uint64_t)((kk >> 2) * 512 + (kk & 3) * 2),
-                      idesc_qk, t2 > 0);
-          }
+        for (int t2 = 0; t2 < 2; ++t2) {
+          const int kk = 2 * g + t2;
+          mma_tmemA(tm + kColS + 64 * b, tm + kColQ + 8 * kk, kd + (uint64_t)((kk >> 2) * 512 + (kk & 3) * 2),
+                    idesc_qk, t2 > 0);
         }
-        if (k == rounds - 1) tc_commit(&ctl->kd_empty[kb]);
-        tc_commit(&ctl->s_full);
+        if (g == kGroups - 1) tc_commit(&ctl->kd_empty[kb]);
+        tc_commit(&ctl->s_full[b]);
         ++rnd;
       }
       return true;
@@ -360,39 +366,37 @@ __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_con
 #pragma unroll
         for (int e = 0; e < 64; ++e) sv[e] = 0u;  // fp32 zero
         const float* ksl = kscale + (i % kSlots) * kSlotFloats;
-        for (int k = 0; k < rounds && !fail; ++k) {
-          if (!waitw(&ctl->s_full, rnd & 1, abort_flag)) {
+        for (int g = 0; g < kGroups && !fail; ++g) {
+          const int sb = rnd % nsb;
+          if (!waitw(&ctl->s_full[sb], (rnd / nsb) & 1, abort_flag)) {
             fail = true;
             break;
           }
           tc_after();
-          for (int gg = 0; gg < gpr; ++gg) {
-            const int g = k * gpr + gg;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              uint32_t t[32];
-              tmem_ld32(lane_addr + kColS + 64 * gg + 32 * half, t);
-              tmem_wait_ld(t);
-              if (gg == gpr - 1 && half == 1) {  // the round's last load: release S
-                tc_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->s_free);
-              }
-              if (p.dots != nullptr && live) {  // inspection: this kernel's own integer dots
-                int32_t* drow = p.dots + (((int64_t)h * R + r) * nkeys + key0 + 32 * half) * kGroups + g;
+          for (int half = 0; half < 2; ++half) {
+            uint32_t t[32];
+            tmem_ld32(lane_addr + kColS + 64 * sb + 32 * half, t);
+            tmem_wait_ld(t);
+            if (half == 1) {  // the round's last load: release the block
+              tc_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&ctl->s_free[sb]);
+            }
+            if (p.dots != nullptr && live) {  // inspection: this kernel's own integer dots
+              int32_t* drow = p.dots + (((int64_t)h * R + r) * nkeys + key0 + 32 * half) * kGroups + g;
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                  if (key0 + 32 * half + e < tok1) drow[(int64_t)e * kGroups] = __float2int_rn(__uint_as_float(t[e]));
-              }
-              const float4* sc4 = reinterpret_cast<const float4*>(ksl + g * kTileTok + 32 * half);
+              for (int e = 0; e < 32; ++e)
+                if (key0 + 32 * half + e < tok1) drow[(int64_t)e * kGroups] = __float2int_rn(__uint_as_float(t[e]));
+            }
+            const float4* sc4 = reinterpret_cast<const float4*>(ksl + g * kTileTok + 32 * half);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float4 x = sc4[e];
-                sv[32 * half + 4 * e] = __float_as_uint(fmaf(x.x, __uint_as_float(t[4 * e]), __uint_as_float(sv[32 * half + 4 * e])));
-                sv[32 * half + 4 * e + 1] = __float_as_uint(fmaf(x.y, __uint_as_float(t[4 * e + 1]), __uint_as_float(sv[32 * half + 4 * e + 1])));
-                sv[32 * half + 4 * e + 2] = __float_as_uint(fmaf(x.z, __uint_as_float(t[4 * e + 2]), __uint_as_float(sv[32 * half + 4 * e + 2])));
-                sv[32 * half + 4 * e + 3] = __float_as_uint(fmaf(x.w, __uint_as_float(t[4 * e + 3]), __uint_as_float(sv[32 * half + 4 * e + 3])));
-              }
+            for (int e = 0; e < 8; ++e) {
+              const float4 x = sc4[e];
+              sv[32 * half + 4 * e] = __float_as_uint(fmaf(x.x, __uint_as_float(t[4 * e]), __uint_as_float(sv[32 * half + 4 * e])));
+              sv[32 * half + 4 * e + 1] = __float_as_uint(fmaf(x.y, __uint_as_float(t[4 * e + 1]), __uint_as_float(sv[32 * half + 4 * e + 1])));
+              sv[32 * half + 4 * e + 2] = __float_as_uint(fmaf(x.z, __uint_as_float(t[4 * e + 2]), __uint_as_float(sv[32 * half + 4 * e + 2])));
+              sv[32 * half + 4 * e + 3] = __float_as_uint(fmaf(x.w, __uint_as_float(t[4 * e + 3]), __uint_as_float(sv[32 * half + 4 * e + 3])));
             }
           }
           ++rnd;
@@ -710,9 +714,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_con
   if (tid == 0 && ctl->abort) report(p.status, STV_DEV_TIMEOUT);
 }
 
-template <bool kAppend>
+template <bool kAppend, bool kWithhold = false>
 cudaError_t launch_one(const VerifyParams& p, cudaStream_t s) {
-  auto kernel = verify_i8_kernel<kAppend>;
+  auto kernel = verify_i8_kernel<kAppend, kWithhold>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   kernel<<<p.n_units, kThreads, kSmemBytes, s>>>(p);
@@ -723,6 +727,7 @@ cudaError_t launch_one(const VerifyParams& p, cudaStream_t s) {
 
 cudaError_t launch_verify_i8(const VerifyParams& p, cudaStream_t s) {
   const bool append = p.k_tree != nullptr && p.v_tree != nullptr;
+  if (p.test_withhold_copies) return launch_one<false, true>(p, s);
   return append ? launch_one<true>(p, s) : launch_one<false>(p, s);
 }
 

@@ -113,7 +113,9 @@ __device__ __forceinline__ bool settle(uint64_t* b, uint32_t parity, uint32_t pr
 
 // kAppend: the round's tree rows are packed into the cache by this launch
 // (stv_append_verify_attn); the plain instantiation carries none of that code.
-template <bool kAppend, bool kI4>
+// kWithhold (failure-path test only, stv_verify_attn_timeout_test): the
+// producer issues no copy, so every wait on one runs out.
+template <bool kAppend, bool kI4, bool kWithhold = false>
 __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_constant__ VerifyParams p) {
   using F = Fmt<kI4>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -195,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
     if (lane == 0) {
       int issued = 0;
       bool tree_ready = !kAppend;
-      for (int i = 0; i < n_tiles; ++i) {
+      for (int i = 0; i < (kWithhold ? 0 : n_tiles); ++i) {
         const int st = i % F::stages;
         if (!wait1(&bars->raw_empty[st], ((i / F::stages) & 1) ^ 1, abort_flag)) break;
         const int key0 = tok0 + i * kTileTok;
@@ -694,8 +696,9 @@ cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s) {
   if (p.path == STV_PATH_INT8 && !p.i4) return launch_verify_i8(p, s);
   const bool append = p.k_tree != nullptr && p.v_tree != nullptr;
   // the fused append packs the 3-bit cache only (the host refuses it for int4)
-  auto kernel = p.i4 ? verify_tc_kernel<false, true>
-                     : (append ? verify_tc_kernel<true, false> : verify_tc_kernel<false, false>);
+  auto kernel = p.test_withhold_copies ? (p.i4 ? verify_tc_kernel<false, true, true> : verify_tc_kernel<false, false, true>)
+                : p.i4 ? verify_tc_kernel<false, true>
+                       : (append ? verify_tc_kernel<true, false> : verify_tc_kernel<false, false>);
   const int smem = p.i4 ? Fmt<true>::smem : Fmt<false>::smem;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

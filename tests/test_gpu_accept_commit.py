@@ -114,3 +114,30 @@ def test_commit_rejects_bad_counts_without_writing(gpu):
     torch.cuda.synchronize()
     assert int(status.item()) & stv.STV_DEV_BAD_COMMIT
     assert torch.equal(before, layer.pool)
+
+
+def test_commit_all_or_nothing_on_bad_page(gpu):
+    """A destination page outside one layer's pool: no layer is written and
+    ctx_dev stays put (STV_DEV_BAD_PAGE); with pages inside every pool the
+    same call commits every layer and advances ctx_dev."""
+    shape = stv.make_shape(24, 4)
+    g = torch.Generator(device="cpu").manual_seed(11)
+    big = stv.LayerCache(torch.randint(0, 256, (6 * 4 * stv.HEAD_BLOCK_BYTES,), generator=g, dtype=torch.uint8).to(gpu), 4)
+    small = stv.LayerCache(torch.randint(0, 256, (3 * 4 * stv.HEAD_BLOCK_BYTES,), generator=g, dtype=torch.uint8).to(gpu), 4)
+    n_commit = torch.tensor([3], dtype=torch.int32, device=gpu)
+    path = torch.tensor([[0, 2, 5, -1, -1, -1, -1, -1]], dtype=torch.int32, device=gpu)
+    for table, bad in (([0, 5], True), ([0, 2], False)):
+        seqs = [stv.Seq(torch.tensor(table, dtype=torch.int32, device=gpu), 300)]  # rows 300.. sit in logical page 1
+        before = [big.pool.clone(), small.pool.clone()]
+        ctx_dev = torch.tensor([300], dtype=torch.int32, device=gpu)
+        status = torch.zeros(1, dtype=torch.int32, device=gpu)
+        stv.stv_kv_commit(shape, [big, small], seqs, 8, n_commit, path, ctx_dev=ctx_dev, dev_status=status)
+        torch.cuda.synchronize()
+        if bad:
+            assert int(status.item()) & stv.STV_DEV_BAD_PAGE
+            assert torch.equal(before[0], big.pool) and torch.equal(before[1], small.pool)
+            assert int(ctx_dev.item()) == 300
+        else:
+            assert int(status.item()) == 0
+            assert not torch.equal(before[0], big.pool) and not torch.equal(before[1], small.pool)
+            assert int(ctx_dev.item()) == 303

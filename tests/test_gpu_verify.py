@@ -51,6 +51,11 @@ def test_chain_workload_all_rows_and_sequential_decode(gpu, path):
         stv.stv_split_combine(r.shape, seqs, 1, ws, o)
         step = o.float().cpu().numpy()[0, 0]
         assert_attention_close(got[0, i][:, None, :], step[:, None, :], f"chain step {i}")
+        # Both launches cut keys [0, 8200) and [0, 8193 + i) into the same
+        # splits (129 tiles of 64 per KV head, 4 tiles per split, 132 work
+        # units), and every row's arithmetic is its own: node i of the chain
+        # equals the one-row decode bit for bit.
+        assert np.array_equal(got[0, i], step), f"chain node {i} differs from its sequential decode"
 
 
 @pytest.mark.parametrize("path", ["exact", "int8"])
@@ -174,3 +179,73 @@ def test_workspace_too_small_rejected(gpu):
     with pytest.raises(stv.StvError) as e:
         stv.stv_verify_attn(r.shape, r.layer, r.seqs, r.q, torch.as_tensor(r.parent, device=gpu), 4, "exact", ws)
     assert e.value.status == stv.STV_ERR_WORKSPACE_TOO_SMALL
+
+
+@pytest.mark.parametrize("path", ["exact", "int8"])
+def test_graph_replay_deterministic(gpu, path):
+    """A round's verify, split merge and acceptance captured once in a CUDA
+    graph and replayed twice give bit-identical outputs, equal to the eager
+    launches' (fixed split order, no float atomics, no data-dependent
+    scheduling)."""
+    r = Round([5000, 300, 12000], 16, seed=61)
+    r.gpu_cache()
+    eager = r.gpu_verify(path)
+    parent = torch.as_tensor(r.parent, device=gpu)
+    draft = torch.as_tensor(r.draft, device=gpu)
+    argmax = torch.as_tensor(r.argmax, device=gpu)
+    ws = torch.empty(stv.stv_verify_workspace_bytes(r.shape, r.seqs, r.T), dtype=torch.uint8, device=gpu)
+    o = torch.empty_like(eager)
+    n_commit = torch.zeros(r.n_seqs, dtype=torch.int32, device=gpu)
+    acc_path = torch.zeros((r.n_seqs, r.T), dtype=torch.int32, device=gpu)
+    out_ids = torch.zeros((r.n_seqs, r.T), dtype=torch.int32, device=gpu)
+
+    def launches():
+        stv.stv_verify_attn(r.shape, r.layer, r.seqs, r.q, parent, r.T, path, ws)
+        stv.stv_split_combine(r.shape, r.seqs, r.T, ws, o)
+        stv.stv_tree_accept(parent, draft, argmax, n_commit, acc_path, out_ids)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        launches()  # warm-up off the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        launches()
+    outs = []
+    for _ in range(2):
+        o.fill_(float("nan"))
+        n_commit.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        outs.append((o.clone(), n_commit.clone(), acc_path.clone(), out_ids.clone()))
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
+    assert torch.equal(outs[0][0], eager)
+
+
+@pytest.mark.parametrize("path", ["exact", "int8"])
+def test_wait_timeout_reported_and_context_usable(gpu, path):
+    """Failure detection without a GPU fault: the verify kernel with its
+    copies withheld (stv_verify_attn_timeout_test) has every consumer's wait
+    run out; the launch returns within seconds with STV_DEV_TIMEOUT, and a
+    normal verify right after it on the same context still matches the
+    oracle."""
+    import time
+
+    r = Round([300], 4, seed=303)
+    r.gpu_cache()
+    r.oracle_cache()
+    ws = torch.empty(stv.stv_verify_workspace_bytes(r.shape, r.seqs, r.T), dtype=torch.uint8, device=gpu)
+    status = torch.zeros(1, dtype=torch.int32, device=gpu)
+    parent = torch.as_tensor(r.parent, device=gpu)
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    stv.stv_verify_attn_timeout_test(r.shape, r.layer, r.seqs, r.q, parent, r.T, path, ws, dev_status=status)
+    torch.cuda.synchronize()
+    elapsed = time.monotonic() - t0
+    assert int(status.item()) & stv.STV_DEV_TIMEOUT
+    assert elapsed < 30.0, elapsed
+    got = r.gpu_verify(path).float().cpu().numpy()
+    assert_attention_close(got, r.oracle_attention(path), f"verify after a timed-out launch ({path})")

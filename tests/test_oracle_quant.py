@@ -179,3 +179,33 @@ def test_int8_q_quantizer_ties_to_even():
     assert sq == pytest.approx(1.0, abs=0)
     qz, sz = oracle.quantize_q_int8(np.zeros(256, np.float16))
     assert qz.tolist() == [0] * 256 and sz == 0.0
+
+
+def test_v_layout_against_hand_derived_positions():
+    """The V half of the page layout: one V entry's code bits and its group
+    scale land at byte positions worked out by hand (tests/golden/v_layout.txt)
+    from the layout statement, for tokens in different pages, tiles, 32-token
+    blocks, KV heads and channel groups (the code-31 case spreads its bits
+    over all three words)."""
+    rows = []
+    for line in open(os.path.join(GOLDEN, "v_layout.txt")):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            rows.append(line.split())
+    assert len(rows) == 4
+    table = np.array([2, 0, 3, 1], np.int32)
+    for pos, head, ch, val, mch, gmax, code, word_off, shift, scale_off, scale_bits in rows:
+        cache = oracle.Cache(4, 4)
+        k = np.zeros((1, 4, 256), np.float16)
+        v = np.zeros((1, 4, 256), np.float16)
+        v[0, int(head), int(mch)] = float(gmax)
+        v[0, int(head), int(ch)] = float(val)
+        oracle.kv_append(cache, [table], k, v, np.zeros(1, np.int32), np.array([int(pos)], np.int32))
+        pool = cache.pool
+        words = pool[int(word_off):int(word_off) + 12].view(np.uint32)
+        if int(shift) == 31:  # code 31: bit b in bit 31 of word b
+            got = sum(((int(words[b]) >> 31) & 1) << b for b in range(3))
+        else:
+            got = (int(words[0]) >> int(shift)) & 7
+        assert got == int(code), (pos, got)
+        assert int(pool[int(scale_off):int(scale_off) + 2].view(np.uint16)[0]) == int(scale_bits, 16), pos
