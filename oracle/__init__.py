@@ -35,6 +35,7 @@ GROUP = 32
 PAGE_TOKENS = 256
 HEAD_BYTES = 57344
 HEAD_BYTES_I4 = 66560  # int4 per token and head (next row f3)
+FORMATS = {"bit3": 0, "int4": 1, "k4v2": 2}  # cache formats (stv_oracle.c): 3-bit; int4 per token-head; K 4 / V 2 bits
 
 
 def build(force: bool = False) -> str:
@@ -68,24 +69,26 @@ def _load():
             lib.orc_block_code.restype = ctypes.c_uint8
             lib.orc_block_code.argtypes = [P, I]
             lib.orc_kv_append.restype = I
-            lib.orc_kv_append.argtypes = [P, I64, I32, I32, P, P, I, P, P, P, P, I]
+            lib.orc_kv_append.argtypes = [P, I64, I32, I32, P, P, I, P, P, P, P, I, I]
             lib.orc_check_tree.restype = I
             lib.orc_check_tree.argtypes = [P, I]
             lib.orc_ancestors.restype = I
             lib.orc_ancestors.argtypes = [P, I, P]
             lib.orc_quantize_q_int8.argtypes = [P, P, P]
             lib.orc_attention.restype = I
-            lib.orc_attention.argtypes = [P, I64, I32, I32, I32, P, P, P, I, P, P, I, I, P, I, P, I]
+            lib.orc_attention.argtypes = [P, I64, I32, I32, I32, P, P, P, I, P, P, I, I, P, I, P, I, I]
             lib.orc_int8_dots.restype = I
-            lib.orc_int8_dots.argtypes = [P, I64, I32, I32, I32, P, P, I, P, I, I64, I64, P]
+            lib.orc_int8_dots.argtypes = [P, I64, I32, I32, I32, P, P, I, P, I, I64, I64, P, I]
             lib.orc_tree_accept.restype = I
             lib.orc_tree_accept.argtypes = [P, P, P, I, P, P, P]
             lib.orc_kv_commit.restype = I
-            lib.orc_kv_commit.argtypes = [P, I64, I32, I32, P, P, P, I, P, P, I]
+            lib.orc_kv_commit.argtypes = [P, I64, I32, I32, P, P, P, I, P, P, I, I]
             lib.orc_decode_rows.restype = I
-            lib.orc_decode_rows.argtypes = [P, I64, I32, I32, P, P, I, I64, I64, I, P]
+            lib.orc_decode_rows.argtypes = [P, I64, I32, I32, P, P, I, I64, I64, I, P, I]
             lib.orc_quantize_row_i4.restype = None
             lib.orc_quantize_row_i4.argtypes = [P, P, P]
+            lib.orc_quantize_group_bits.restype = None
+            lib.orc_quantize_group_bits.argtypes = [P, I, P, P]
             lib.orc_lookup_draft.restype = I
             lib.orc_lookup_draft.argtypes = [P, I64, I, I, I, P, P, P, P]
             _lib = lib
@@ -176,13 +179,16 @@ def check_tree(parent) -> bool:
 
 class Cache:
     """A host-side paged cache for one layer (bytes as uint8): the 3-bit cache
-    (bits=3) or the int4 per-token-head cache (bits=4); the C side tells them
-    apart by the page stride."""
+    (bits=3), the int4 per-token-head cache (bits=4) or the K 4 / V 2-bit
+    cache (kind="k4v2"); every call names the format to the C side."""
 
-    def __init__(self, hkv: int, pool_pages: int, pool: np.ndarray | None = None, bits: int = 3):
+    def __init__(self, hkv: int, pool_pages: int, pool: np.ndarray | None = None, bits: int = 3,
+                 kind: str | None = None):
         self.hkv = int(hkv)
         self.bits = int(bits)
-        self.page_bytes = self.hkv * (HEAD_BYTES if bits == 3 else HEAD_BYTES_I4)
+        self.kind = kind or ("bit3" if bits == 3 else "int4")
+        self.fmt = FORMATS[self.kind]
+        self.page_bytes = self.hkv * (HEAD_BYTES_I4 if self.kind == "int4" else HEAD_BYTES)
         self.pool_pages = int(pool_pages)
         if pool is None:
             pool = np.zeros(self.page_bytes * self.pool_pages, np.uint8)
@@ -209,7 +215,7 @@ def kv_append(cache: Cache, page_tables, k16, v16, row_seq, row_pos):
     assert k.size == n * cache.hkv * HEAD_DIM and v.size == k.size
     _check(
         _load().orc_kv_append(_p(cache.pool), cache.page_bytes, cache.pool_pages, cache.hkv, _p(flat),
-                              _p(offs), len(page_tables), _p(k), _p(v), _p(rs), _p(rp), n),
+                              _p(offs), len(page_tables), _p(k), _p(v), _p(rs), _p(rp), n, cache.fmt),
         "kv_append",
     )
 
@@ -220,7 +226,7 @@ def decode(cache: Cache, page_tables, seq: int, tok_begin: int, tok_end: int, wh
     out = np.zeros((tok_end - tok_begin, cache.hkv, HEAD_DIM), np.float64)
     _check(
         _load().orc_decode_rows(_p(cache.pool), cache.page_bytes, cache.pool_pages, cache.hkv, _p(flat), _p(offs),
-                                int(seq), int(tok_begin), int(tok_end), 0 if which == "k" else 1, _p(out)),
+                                int(seq), int(tok_begin), int(tok_end), 0 if which == "k" else 1, _p(out), cache.fmt),
         "decode",
     )
     return out
@@ -247,7 +253,7 @@ def attention(cache: Cache, page_tables, ctx, q16, parent, hq: int, path: str, r
     _check(
         _load().orc_attention(_p(cache.pool), cache.page_bytes, cache.pool_pages, int(hq), cache.hkv, _p(flat),
                               _p(offs), _p(ctx_a), n_seqs, _p(q), _p(par), t, 0 if path == "exact" else 1,
-                              _p(r), len(r), _p(out), int(n_threads)),
+                              _p(r), len(r), _p(out), int(n_threads), cache.fmt),
         "attention",
     )
     if full:
@@ -263,7 +269,7 @@ def int8_dots(cache: Cache, page_tables, seq: int, q_row16, qhead: int, hq: int,
     out = np.zeros((tok_end - tok_begin, 8), np.int32)
     _check(
         _load().orc_int8_dots(_p(cache.pool), cache.page_bytes, cache.pool_pages, int(hq), cache.hkv, _p(flat),
-                              _p(offs), int(seq), _p(q), int(qhead), int(tok_begin), int(tok_end), _p(out)),
+                              _p(offs), int(seq), _p(q), int(qhead), int(tok_begin), int(tok_end), _p(out), cache.fmt),
         "int8_dots",
     )
     return out
@@ -291,7 +297,7 @@ def kv_commit(cache: Cache, page_tables, ctx, n_commit, path, t: int):
     pth = _i32(path).reshape(len(c), t)
     _check(
         _load().orc_kv_commit(_p(cache.pool), cache.page_bytes, cache.pool_pages, cache.hkv, _p(flat), _p(offs),
-                              _p(c), len(c), _p(n), _p(pth), int(t)),
+                              _p(c), len(c), _p(n), _p(pth), int(t), cache.fmt),
         "kv_commit",
     )
 
@@ -320,4 +326,15 @@ def quantize_row_i4(x):
     s = np.zeros(1, np.uint16)
     u = np.zeros(HEAD_DIM, np.uint8)
     _load().orc_quantize_row_i4(_p(xh), _p(s), _p(u))
+    return s[0], u
+
+
+def quantize_group_bits(x, bits: int):
+    """The b-bit group quantizer (stv_oracle.c, orc_quantize_group_bits): 32
+    fp16 values -> (fp16 scale bits, codes u = c + 2^(b-1))."""
+    xh = np.ascontiguousarray(np.asarray(x, np.float16).view(np.uint16))
+    assert xh.size == GROUP
+    s = np.zeros(1, np.uint16)
+    u = np.zeros(GROUP, np.uint8)
+    _load().orc_quantize_group_bits(_p(xh), int(bits), _p(s), _p(u))
     return s[0], u

@@ -165,6 +165,55 @@ void orc_quantize_row_i4(const uint16_t* x, uint16_t* s_out, uint8_t* u) {
   *s_out = s;
 }
 
+/* ------------------------------------------------------------------------
+ * Third cache format (next row f3): the KVarN-style 4/2-bit cache (Reddit
+ * posts (u/iamMess), "Now added" list: a KVarN 4/2-bit KV cache; syv-ai
+ * README (mirror), DFlash2 at 240k: CTX=huge uses it).  The pages name it
+ * and give its cost, not its quantizer.  Reading: the 3-bit cache's
+ * quantizer at other widths, 4 bits for K and 2 bits for V, one fp16 scale
+ * per (token, KV head, group of 32 channels): for b bits, h = 2^(b-1),
+ * s = fp16(m / h), c = clamp(rne(x / s), -h, h - 1) (all 0 when s == 0),
+ * stored as u = c + h; decoded value s * c.  (At b = 3 this is the 3-bit
+ * cache's quantizer, whose code is u.)  Layout per KV head (57,344 bytes,
+ * the 3-bit cache's size: 4 + 2 bits against 3 + 3):
+ *   [0, 32768)      K codes  [256 tok][8 groups][4 words]; a word holds 8
+ *                   channels, element e at bit 4*(e/2) + 16*(e%2)
+ *   [32768, 36864)  K scales [256 tok][8 groups] fp16
+ *   [36864, 53248)  V codes  [4 tiles of 64 tok][256 ch][4 words]; a word
+ *                   holds one channel's codes for 16 tokens, token t at
+ *                   bit 2*(t/2) + 16*(t%2)
+ *   [53248, 57344)  V scales [4 tiles][8 groups][64 tok] fp16 (as in the
+ *                   3-bit cache)
+ * Its page stride equals the 3-bit cache's, so callers name the format.
+ */
+#define KV2_OFF_K_CODES 0
+#define KV2_OFF_K_SCALES (PAGE_TOK * N_GROUPS * 16)                  /* 32768 */
+#define KV2_OFF_V_CODES (KV2_OFF_K_SCALES + PAGE_TOK * N_GROUPS * 2)  /* 36864 */
+#define KV2_OFF_V_SCALES (KV2_OFF_V_CODES + PAGE_TOK * HEAD_DIM / 4)  /* 53248 */
+#define KV2_HEAD_BYTES (KV2_OFF_V_SCALES + PAGE_TOK * N_GROUPS * 2)   /* 57344 */
+
+/* Bit position of token t (0..15) inside a 2-bit V word. */
+static int v2_pos(int t) { return ((t & 1) ? 16 : 0) + 2 * (t >> 1); }
+
+/* Quantize 32 fp16 values at b bits: one fp16 scale and codes u = c + h. */
+void orc_quantize_group_bits(const uint16_t* x, int bits, uint16_t* s_out, uint8_t* u) {
+  const double h = (double)(1 << (bits - 1));
+  double m = 0.0;
+  for (int i = 0; i < GROUP; ++i) {
+    double a = fabs(orc_half_to_double(x[i]));
+    if (a > m) m = a;
+  }
+  uint16_t s = orc_double_to_half(m / h);
+  double sd = orc_half_to_double(s);
+  for (int i = 0; i < GROUP; ++i) {
+    double c = sd == 0.0 ? 0.0 : rint(orc_half_to_double(x[i]) / sd);
+    if (c < -h) c = -h;
+    if (c > h - 1.0) c = h - 1.0;
+    u[i] = (uint8_t)(c + h);
+  }
+  *s_out = s;
+}
+
 /* ------------------------------------------------------------------------ */
 /* 3-bit group quantizer and the block bit layout.                          */
 /* ------------------------------------------------------------------------ */
@@ -244,21 +293,16 @@ typedef struct {
   int32_t hkv;
   const int32_t* page_tables; /* all sequences' tables, concatenated */
   const int32_t* pt_offsets;  /* [n_seqs + 1] */
-  int fmt;                    /* 0: 3-bit groups of 32, 1: int4 per token and head */
+  int fmt;                    /* 0: 3-bit groups of 32, 1: int4 per token and head, 2: K 4 bits / V 2 bits */
   int64_t head_bytes;
 } cache_view;
 
-/* The pool's format from its page stride; ORC_BAD_ARG if it is neither. */
-static int view_format(cache_view* cv) {
-  if (cv->page_bytes == (int64_t)cv->hkv * HEAD_BYTES) {
-    cv->fmt = 0;
-    cv->head_bytes = HEAD_BYTES;
-  } else if (cv->page_bytes == (int64_t)cv->hkv * I4_HEAD_BYTES) {
-    cv->fmt = 1;
-    cv->head_bytes = I4_HEAD_BYTES;
-  } else {
-    return ORC_BAD_ARG;
-  }
+/* Set the pool's format; ORC_BAD_ARG if the page stride does not match it. */
+static int view_format(cache_view* cv, int fmt) {
+  static const int64_t head[3] = {HEAD_BYTES, I4_HEAD_BYTES, KV2_HEAD_BYTES};
+  if (fmt < 0 || fmt > 2 || cv->page_bytes != (int64_t)cv->hkv * head[fmt]) return ORC_BAD_ARG;
+  cv->fmt = fmt;
+  cv->head_bytes = head[fmt];
   return ORC_OK;
 }
 
@@ -309,10 +353,37 @@ static uint8_t* i4_scale(uint8_t* hb, int which, int slot) {
   return hb + (which == 0 ? I4_OFF_K_SCALES : I4_OFF_V_SCALES) + slot * 2;
 }
 
+/* K 4 / V 2-bit cache: code u of channel `ch` of one token and head. */
+static uint8_t* kv2_k_word(uint8_t* hb, int slot, int ch) {
+  return hb + KV2_OFF_K_CODES + slot * 128 + (ch / GROUP) * 16 + ((ch % GROUP) / 8) * 4;
+}
+static uint8_t* kv2_v_word(uint8_t* hb, int slot, int ch) {
+  int within = slot % TILE_TOK;
+  return hb + KV2_OFF_V_CODES + (slot / TILE_TOK) * (HEAD_DIM * 16) + ch * 16 + (within / 16) * 4;
+}
+static int kv2_code(uint8_t* hb, int which, int slot, int ch) {
+  uint32_t w;
+  if (which == 0) {
+    memcpy(&w, kv2_k_word(hb, slot, ch), 4);
+    return (int)((w >> i4_pos(ch % 8)) & 15u);
+  }
+  memcpy(&w, kv2_v_word(hb, slot, ch), 4);
+  return (int)((w >> v2_pos(slot % 16)) & 3u);
+}
+static uint8_t* kv2_k_scale(uint8_t* hb, int slot, int g) { return hb + KV2_OFF_K_SCALES + slot * 16 + g * 2; }
+
 static int decode_row(const cache_view* cv, int seq, int64_t tok, int h, int which, double* out) {
   uint8_t* hb = head_block(cv, seq, tok, h);
   if (!hb) return ORC_BAD_PAGE;
   int slot = (int)(tok % PAGE_TOK);
+  if (cv->fmt == 2) {
+    for (int g = 0; g < N_GROUPS; ++g) {
+      double s = orc_half_to_double(load_u16(which == 0 ? kv2_k_scale(hb, slot, g) : v_scale(hb, slot, g)));
+      for (int i = 0; i < GROUP; ++i)
+        out[g * GROUP + i] = s * (kv2_code(hb, which, slot, g * GROUP + i) - (which == 0 ? 8 : 2));
+    }
+    return ORC_OK;
+  }
   if (cv->fmt == 1) {
     double s = orc_half_to_double(load_u16(i4_scale(hb, which, slot)));
     for (int c = 0; c < HEAD_DIM; ++c) out[c] = s * (i4_code(hb, which, slot, c) - 8);
@@ -336,13 +407,19 @@ static int decode_row(const cache_view* cv, int seq, int64_t tok, int h, int whi
   return ORC_OK;
 }
 
-/* K's integer values (code - 4 for the 3-bit cache, u - 8 for int4) and
+/* K's integer values (code - 4 for the 3-bit cache, u - 8 for int4 and for
+ * the 4-bit K of the K 4 / V 2-bit cache) and
  * per-group scales of one token and head, for the int8 definition (the
  * int4 cache has one scale per token: every group gets it). */
 static int k_codes_row(const cache_view* cv, int seq, int64_t tok, int h, int8_t* kv, double* scales) {
   uint8_t* hb = head_block(cv, seq, tok, h);
   if (!hb) return ORC_BAD_PAGE;
   int slot = (int)(tok % PAGE_TOK);
+  if (cv->fmt == 2) {
+    for (int g = 0; g < N_GROUPS; ++g) scales[g] = orc_half_to_double(load_u16(kv2_k_scale(hb, slot, g)));
+    for (int c = 0; c < HEAD_DIM; ++c) kv[c] = (int8_t)(kv2_code(hb, 0, slot, c) - 8);
+    return ORC_OK;
+  }
   if (cv->fmt == 1) {
     double s = orc_half_to_double(load_u16(i4_scale(hb, 0, slot)));
     for (int g = 0; g < N_GROUPS; ++g) scales[g] = s;
@@ -365,9 +442,9 @@ static int k_codes_row(const cache_view* cv, int seq, int64_t tok, int h, int8_t
 int orc_kv_append(uint8_t* pool, int64_t page_bytes, int32_t pool_pages, int32_t hkv,
                   const int32_t* page_tables, const int32_t* pt_offsets, int n_seqs,
                   const uint16_t* k, const uint16_t* v, /* [n_rows][hkv][256] */
-                  const int32_t* row_seq, const int32_t* row_pos, int n_rows) {
+                  const int32_t* row_seq, const int32_t* row_pos, int n_rows, int fmt) {
   cache_view cv = {pool, page_bytes, pool_pages, hkv, page_tables, pt_offsets};
-  if (view_format(&cv) != ORC_OK) return ORC_BAD_ARG;
+  if (view_format(&cv, fmt) != ORC_OK) return ORC_BAD_ARG;
   for (int r = 0; r < n_rows; ++r) {
     int seq = row_seq[r];
     if (seq < 0 || seq >= n_seqs) return ORC_BAD_ARG;
@@ -377,6 +454,29 @@ int orc_kv_append(uint8_t* pool, int64_t page_bytes, int32_t pool_pages, int32_t
       int slot = row_pos[r] % PAGE_TOK;
       const uint16_t* kr = k + ((int64_t)r * hkv + h) * HEAD_DIM;
       const uint16_t* vr = v + ((int64_t)r * hkv + h) * HEAD_DIM;
+      if (cv.fmt == 2) { /* K 4 bits, V 2 bits, per group of 32 channels */
+        for (int g = 0; g < N_GROUPS; ++g) {
+          uint16_t s;
+          uint8_t u[GROUP];
+          orc_quantize_group_bits(kr + g * GROUP, 4, &s, u);
+          for (int wd = 0; wd < 4; ++wd) {
+            uint32_t w = 0;
+            for (int e = 0; e < 8; ++e) w |= (uint32_t)u[8 * wd + e] << i4_pos(e);
+            memcpy(kv2_k_word(hb, slot, g * GROUP + 8 * wd), &w, 4);
+          }
+          store_u16(kv2_k_scale(hb, slot, g), s);
+          orc_quantize_group_bits(vr + g * GROUP, 2, &s, u);
+          store_u16(v_scale(hb, slot, g), s);
+          for (int i = 0; i < GROUP; ++i) {
+            uint8_t* p = kv2_v_word(hb, slot, g * GROUP + i);
+            uint32_t w;
+            memcpy(&w, p, 4);
+            w = (w & ~(3u << v2_pos(slot % 16))) | ((uint32_t)u[i] << v2_pos(slot % 16));
+            memcpy(p, &w, 4);
+          }
+        }
+        continue;
+      }
       if (cv.fmt == 1) { /* int4 per token and head */
         uint16_t s;
         uint8_t u[HEAD_DIM];
@@ -586,12 +686,12 @@ static void* attn_worker(void* arg) {
 int orc_attention(const uint8_t* pool, int64_t page_bytes, int32_t pool_pages, int32_t hq, int32_t hkv,
                   const int32_t* page_tables, const int32_t* pt_offsets, const int32_t* ctx, int n_seqs,
                   const uint16_t* q, const int32_t* parent, int t, int path, const int32_t* rows, int n_rows,
-                  double* out, int n_threads) {
+                  double* out, int n_threads, int fmt) {
   if (hkv < 1 || hq % hkv != 0 || t < 1 || t > 32 || (path != 0 && path != 1)) return ORC_BAD_ARG;
   for (int r = 0; r < n_rows; ++r)
     if (rows[3 * r] < 0 || rows[3 * r] >= n_seqs) return ORC_BAD_ARG;
   cache_view cv = {(uint8_t*)pool, page_bytes, pool_pages, hkv, page_tables, pt_offsets};
-  if (view_format(&cv) != ORC_OK) return ORC_BAD_ARG;
+  if (view_format(&cv, fmt) != ORC_OK) return ORC_BAD_ARG;
   attn_job jb;
   jb.cv = &cv;
   jb.ctx = ctx;
@@ -623,9 +723,9 @@ int orc_attention(const uint8_t* pool, int64_t page_bytes, int32_t pool_pages, i
  * out: [tok_end - tok_begin][8] int32 (|I_g| <= 32*127*4 fits easily). */
 int orc_int8_dots(const uint8_t* pool, int64_t page_bytes, int32_t pool_pages, int32_t hq, int32_t hkv,
                   const int32_t* page_tables, const int32_t* pt_offsets, int seq, const uint16_t* qrow,
-                  int qhead, int64_t tok_begin, int64_t tok_end, int32_t* out) {
+                  int qhead, int64_t tok_begin, int64_t tok_end, int32_t* out, int fmt) {
   cache_view cv = {(uint8_t*)pool, page_bytes, pool_pages, hkv, page_tables, pt_offsets};
-  if (view_format(&cv) != ORC_OK) return ORC_BAD_ARG;
+  if (view_format(&cv, fmt) != ORC_OK) return ORC_BAD_ARG;
   int h = qhead / (hq / hkv);
   int8_t qi[HEAD_DIM];
   float sq;
@@ -700,13 +800,43 @@ int orc_tree_accept(const int32_t* parent, const int32_t* draft, const int32_t* 
 
 int orc_kv_commit(uint8_t* pool, int64_t page_bytes, int32_t pool_pages, int32_t hkv, const int32_t* page_tables,
                   const int32_t* pt_offsets, const int32_t* ctx, int n_seqs, const int32_t* n_commit,
-                  const int32_t* path, int t) {
+                  const int32_t* path, int t, int fmt) {
   cache_view cv = {pool, page_bytes, pool_pages, hkv, page_tables, pt_offsets};
-  if (view_format(&cv) != ORC_OK) return ORC_BAD_ARG;
+  if (view_format(&cv, fmt) != ORC_OK) return ORC_BAD_ARG;
   for (int s = 0; s < n_seqs; ++s) {
     int n = n_commit[s];
     if (n < 1 || n > t) return ORC_BAD_ARG;
     for (int h = 0; h < hkv; ++h) {
+      if (cv.fmt == 2) { /* K 4 / V 2: K codes and both scale rows move whole; V codes channel by channel */
+        uint8_t kc2[32][128], ks2[32][16], vs2[32][16], vu2[32][HEAD_DIM];
+        for (int i = 0; i < n; ++i) {
+          int64_t src = (int64_t)ctx[s] + path[(int64_t)s * t + i];
+          uint8_t* hb = head_block(&cv, s, src, h);
+          if (!hb) return ORC_BAD_PAGE;
+          int slot = (int)(src % PAGE_TOK);
+          memcpy(kc2[i], hb + KV2_OFF_K_CODES + slot * 128, 128);
+          memcpy(ks2[i], kv2_k_scale(hb, slot, 0), 16);
+          for (int g = 0; g < N_GROUPS; ++g) memcpy(vs2[i] + 2 * g, v_scale(hb, slot, g), 2);
+          for (int c = 0; c < HEAD_DIM; ++c) vu2[i][c] = (uint8_t)kv2_code(hb, 1, slot, c);
+        }
+        for (int i = 0; i < n; ++i) {
+          int64_t dst = (int64_t)ctx[s] + i;
+          uint8_t* hb = head_block(&cv, s, dst, h);
+          if (!hb) return ORC_BAD_PAGE;
+          int slot = (int)(dst % PAGE_TOK);
+          memcpy(hb + KV2_OFF_K_CODES + slot * 128, kc2[i], 128);
+          memcpy(kv2_k_scale(hb, slot, 0), ks2[i], 16);
+          for (int g = 0; g < N_GROUPS; ++g) memcpy(v_scale(hb, slot, g), vs2[i] + 2 * g, 2);
+          for (int c = 0; c < HEAD_DIM; ++c) {
+            uint8_t* p = kv2_v_word(hb, slot, c);
+            uint32_t w;
+            memcpy(&w, p, 4);
+            w = (w & ~(3u << v2_pos(slot % 16))) | ((uint32_t)vu2[i][c] << v2_pos(slot % 16));
+            memcpy(p, &w, 4);
+          }
+        }
+        continue;
+      }
       if (cv.fmt == 1) { /* int4: K codes and both scales move whole; V nibbles channel by channel */
         uint8_t kc4[32][128], sc4[32][4], vu[32][HEAD_DIM];
         for (int i = 0; i < n; ++i) {
@@ -778,9 +908,9 @@ int orc_kv_commit(uint8_t* pool, int64_t page_bytes, int32_t pool_pages, int32_t
 /* Decode helpers exported for the tests. */
 int orc_decode_rows(const uint8_t* pool, int64_t page_bytes, int32_t pool_pages, int32_t hkv,
                     const int32_t* page_tables, const int32_t* pt_offsets, int seq, int64_t tok_begin,
-                    int64_t tok_end, int which, double* out /* [n_tok][hkv][256] */) {
+                    int64_t tok_end, int which, double* out /* [n_tok][hkv][256] */, int fmt) {
   cache_view cv = {(uint8_t*)pool, page_bytes, pool_pages, hkv, page_tables, pt_offsets};
-  if (view_format(&cv) != ORC_OK) return ORC_BAD_ARG;
+  if (view_format(&cv, fmt) != ORC_OK) return ORC_BAD_ARG;
   for (int64_t j = tok_begin; j < tok_end; ++j)
     for (int h = 0; h < hkv; ++h) {
       int rc = decode_row(&cv, seq, j, h, which, out + ((j - tok_begin) * hkv + h) * HEAD_DIM);
