@@ -48,8 +48,9 @@ UNIT = "us/layer-round"
 
 # Packed bytes per token and KV head, K + V: the 3-bit cache holds 96 B of
 # codes and 16 B of fp16 group scales for each; the int4 per-token-head cache
-# 128 B of codes and one 2 B scale.
-KV_FORMATS = {"bit3": (32, 2 * (96 + 16)), "int4": (256, 2 * (128 + 2))}
+# 128 B of codes and one 2 B scale; the K 4 / V 2-bit cache 128 B (K) and
+# 64 B (V) of codes and 16 B of group scales each.
+KV_FORMATS = {"bit3": (32, 2 * (96 + 16)), "int4": (256, 2 * (128 + 2)), "k4v2": (32, (128 + 16) + (64 + 16))}
 
 
 def algorithmic_bytes_per_layer_round(ctx_list, t, hq=24, hkv=4, kv_format="bit3"):
@@ -200,7 +201,7 @@ class GpuRound:
     """All layers of one workload resident on the GPU, plus one round's inputs."""
 
     def __init__(self, w: workloads.Workload, p_accept: float, device, layers: int | None = None,
-                 fuse_append: bool = False, group: int = 32):
+                 fuse_append: bool = False, group: int = 32, kv_format: int = 0):
         import torch
 
         import speculative_tree_verify_bit_gb300 as stv
@@ -209,7 +210,7 @@ class GpuRound:
         self.fuse_append = fuse_append
         self.L = layers or w.layers
         self.T, self.hq, self.hkv = w.t_nodes, w.hq, w.hkv
-        self.shape = stv.make_shape(self.hq, self.hkv, group)
+        self.shape = stv.make_shape(self.hq, self.hkv, group, kv_format)
         self.pool_pages, tables = workloads.page_tables_for(w)
         self.tables = tables
         self.seqs = [stv.Seq(torch.as_tensor(t, device=device), c) for t, c in zip(tables, w.ctx)]
@@ -382,14 +383,18 @@ def measure_prefill(dev, n: int = 32768, reps: int = 3, hq: int = 24, hkv: int =
             "bound": "tensor", "tflops": tflops, "peak_tflops": peak, "frac": tflops / peak, "peak_source": kind}
 
 
-def measure_int4(w: workloads.Workload, p_accept: float, dev, path: str = "exact", reps: int = 10):
-    """The same round over the int4 per-token-head cache (group 256): two
-    layers resident, eager rounds with events around each verify launch; the
-    layers alternate, so a launch does not find its cache in L2 (one layer's
-    cache is larger than L2 at 262K)."""
+def measure_format(w: workloads.Workload, p_accept: float, dev, kind: str, path: str = "exact", reps: int = 10):
+    """The same round over another cache format (the int4 per-token-head
+    cache, or the K 4 / V 2-bit cache): two layers resident, eager rounds with
+    events around each verify launch; the layers alternate, so a launch does
+    not find its cache in L2 (one layer's cache is larger than L2 at 262K)."""
     import torch
 
-    r = GpuRound(w, p_accept, dev, layers=2, group=256)
+    import speculative_tree_verify_bit_gb300 as stv
+
+    group = KV_FORMATS[kind][0]
+    r = GpuRound(w, p_accept, dev, layers=2, group=group,
+                 kv_format=stv.STV_KV_K4V2 if kind == "k4v2" else stv.STV_KV_BY_GROUP)
     for _ in range(3):
         r.step(path)
     torch.cuda.synchronize()
@@ -405,13 +410,15 @@ def measure_int4(w: workloads.Workload, p_accept: float, dev, path: str = "exact
         rounds.append(a.elapsed_time(b))
     st = int(r.status.item())
     v_us = statistics.median(times) * 1e3
-    vbytes = verify_kernel_bytes(w.ctx, w.t_nodes, w.hq, w.hkv, "int4")
-    peak, kind = measured_peak()
+    vbytes = verify_kernel_bytes(w.ctx, w.t_nodes, w.hq, w.hkv, kind)
+    peak, pkind = measured_peak()
+    tf, _ = measured_bf16_peak()
+    vflops = verify_kernel_flops(w.ctx, w.t_nodes, w.hq)
     gbs = vbytes / (v_us * 1e-6) / 1e9
-    out = {"workload": w.name, "group": 256, "path": path, "verify_us_per_launch": v_us,
+    out = {"workload": w.name, "kv_format": kind, "group": group, "path": path, "verify_us_per_launch": v_us,
            "eager_us_per_layer_round": statistics.median(rounds) * 1e3 / r.L, "bound": "hbm",
            "algorithmic_bytes_per_launch": vbytes, "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak,
-           "peak_source": kind, "dev_status": st}
+           "tensor_frac": vflops / (v_us * 1e-6) / 1e12 / tf, "peak_source": pkind, "dev_status": st}
     del r
     torch.cuda.empty_cache()
     return out
@@ -520,7 +527,7 @@ def run_gpu(args, rank, world):
     w = workloads.WORKLOADS[args.workload]
     p_accept = default_p_accept(args, w)
     r = GpuRound(w, p_accept, dev, layers=args.layers, fuse_append=args.fuse_append,
-                 group=KV_FORMATS[args.kv_format][0])
+                 group=KV_FORMATS[args.kv_format][0], kv_format=2 if args.kv_format == "k4v2" else 0)
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -577,7 +584,8 @@ def run_gpu(args, rank, world):
         r.set_trees(p_accept)
     lookup = measure_lookup(w, dev) if extra else None
     prefill = measure_prefill(dev) if extra else None
-    int4 = measure_int4(w, p_accept, dev, args.path) if extra and args.kv_format == "bit3" else None
+    int4 = measure_format(w, p_accept, dev, "int4", args.path) if extra and args.kv_format == "bit3" else None
+    k4v2 = measure_format(w, p_accept, dev, "k4v2") if extra and args.kv_format == "bit3" else None
     if configs:
         del r
         torch.cuda.empty_cache()
@@ -606,7 +614,7 @@ def run_gpu(args, rank, world):
                 vflops=vflops, peak=peak, peak_kind=peak_kind, achieved=achieved, clocks=clocks, status=st,
                 h2d=h2d, d2h=d2h, launches=launches_per_step(args, w) * args.steps, p_accept=p_accept,
                 traffic=traffic, round_gbs=bytes_lr / (us_per_lr * 1e-6) / 1e9 / world, lookup=lookup,
-                prefill=prefill, int4=int4, configs=configs)
+                prefill=prefill, int4=int4, k4v2=k4v2, configs=configs)
 
 
 KERNEL_SOURCES = {  # the files a verify launch's code comes from, per path and cache format
@@ -660,7 +668,7 @@ def oracle_sample(w: workloads.Workload, n_rows: int, threads: int, kv_format: s
 
     T, hq, hkv = w.t_nodes, w.hq, w.hkv
     pool_pages, tables = workloads.page_tables_for(w)
-    cache = oracle.Cache(hkv, pool_pages, bits=3 if kv_format == "bit3" else 4)
+    cache = oracle.Cache(hkv, pool_pages, bits=4 if kv_format == "int4" else 3, kind=kv_format)
     seed = workloads.layer_seed(w, 0)
     # the sample covers the largest sequence (the long-context share dominates)
     s = int(np.argmax(w.ctx))
@@ -692,7 +700,9 @@ def arm_config(args, w: workloads.Workload, p_accept: float, world: int) -> dict
             "l2": "inputs larger than L2 (16 layers of packed KV)", "parallelism": f"replicas{world}",
             "timing": "median over steps of one CUDA-graph replay of the round, CUDA events",
             "append": "fused into verify" if args.fuse_append else "separate launch",
-            "kv_format": {"bit3": "3-bit codes, fp16 scale per 32-group", "int4": "int4 codes, fp16 scale per token and KV head"}[args.kv_format]}
+            "kv_format": {"bit3": "3-bit codes, fp16 scale per 32-group",
+                          "int4": "int4 codes, fp16 scale per token and KV head",
+                          "k4v2": "K 4-bit / V 2-bit codes, fp16 scale per 32-group"}[args.kv_format]}
 
 
 def default_p_accept(args, w: workloads.Workload) -> float:
@@ -741,13 +751,17 @@ def main():
                          "with their own launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kv-format", default="bit3", choices=sorted(KV_FORMATS),
-                    help="cache format: the 3-bit cache (default) or the int4 per-token-head cache")
+                    help="cache format: the 3-bit cache (default), the int4 per-token-head cache or the "
+                         "K 4 / V 2-bit cache")
     ap.add_argument("--no-next-rows", action="store_true",
-                    help="skip the lookup, prefill and int4 measurements (profiling captures)")
+                    help="skip the other configs, lookup, prefill and other-format measurements "
+                         "(profiling captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.fuse_append and args.kv_format != "bit3":
         ap.error("--fuse-append packs the 3-bit cache only")
+    if args.path == "int8" and args.kv_format == "k4v2":
+        ap.error("the K 4 / V 2-bit cache runs the exact path only")
 
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
@@ -800,7 +814,7 @@ def main():
         "dev_status": res["status"],
         "configs": res["configs"],
         "next_rows": {"lookup_draft": res.get("lookup"), "prefill_attn": res.get("prefill"),
-                      "int4_cache_verify": res.get("int4")},
+                      "int4_cache_verify": res.get("int4"), "k4v2_cache_verify": res.get("k4v2")},
     }
     print(json.dumps(line), flush=True)
 

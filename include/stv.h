@@ -92,6 +92,12 @@ enum stv_dev_status {
 
 enum stv_path { STV_PATH_EXACT = 0, STV_PATH_INT8 = 1 };
 
+/* Cache formats (stv_shape.kv_format). */
+enum stv_kv_format {
+  STV_KV_BY_GROUP = 0, /* by stv_shape.group: 32 the 3-bit cache, 256 the int4 per-token-head cache */
+  STV_KV_K4V2 = 2,     /* the KVarN-style cache: K 4 bits, V 2 bits, group 32 (see the notes below) */
+};
+
 typedef struct {
   int32_t hq;          /* query heads (24 for the pages' model) */
   int32_t hkv;         /* KV heads (4) */
@@ -103,12 +109,13 @@ typedef struct {
                         *       per token and KV head (next row f3; see the
                         *       int4 notes below) */
   int32_t page_tokens; /* must be 256 */
+  int32_t kv_format;   /* STV_KV_BY_GROUP, or STV_KV_K4V2 with group 32 */
 } stv_shape;
 
 typedef struct {
   uint8_t* pool;      /* device: n_pages * page_bytes bytes */
-  int64_t page_bytes; /* must equal hkv * STV_HEAD_BLOCK_BYTES (group 32) or
-                       * hkv * STV_HEAD_BLOCK_BYTES_INT4 (group 256) */
+  int64_t page_bytes; /* must equal hkv * STV_HEAD_BLOCK_BYTES (group 32, both
+                       * formats) or hkv * STV_HEAD_BLOCK_BYTES_INT4 (group 256) */
   int32_t n_pages;
 } stv_layer_cache;
 
@@ -138,6 +145,24 @@ int stv_version(void);
  * stv_split_combine, stv_verify_attn_no_alloc, stv_prefill_attn and
  * stv_kv_commit accept it; stv_append_verify_attn and stv_int8_qk_dots return
  * STV_ERR_UNIMPLEMENTED for it. */
+/* The KVarN-style 4/2-bit cache (STV_KV_K4V2, group 32; Reddit posts
+ * (u/iamMess), "Now added" list: KVarN 4/2-bit KV cache; syv-ai README
+ * (mirror), DFlash2 at 240k: CTX=huge; the pages give no formula).  Reading:
+ * the 3-bit cache's quantizer at other widths, per (token, KV head, group of
+ * 32 channels): at b bits, h = 2^(b-1), s = fp16(max|x| / h),
+ * c = clamp(rne(x / s), -h, h - 1), stored as u = c + h; decoded s * c.  K at
+ * 4 bits, V at 2 bits.  Per KV head (57,344 bytes, as the 3-bit cache):
+ *    [0, 32768)      K codes  [256 tokens][8 groups][4 x uint32]; a word holds
+ *                    8 channels, element e at bit 4 * (e / 2) + 16 * (e % 2)
+ *    [32768, 36864)  K scales [256 tokens][8 groups] fp16
+ *    [36864, 53248)  V codes  [4 tiles of 64 tokens][256 channels][4 x uint32];
+ *                    a word holds one channel's codes for 16 tokens, token
+ *                    t at bit 2 * (t / 2) + 16 * (t % 2)
+ *    [53248, 57344)  V scales [4 tiles][8 groups][64 tokens] fp16
+ * stv_kv_append_pack, stv_verify_attn (exact path), stv_split_combine,
+ * stv_verify_attn_no_alloc, stv_prefill_attn (exact path) and stv_kv_commit
+ * accept it; the int8 path, stv_append_verify_attn and stv_int8_qk_dots
+ * return STV_ERR_UNIMPLEMENTED for it. */
 int stv_page_bytes(const stv_shape* shape, int64_t* bytes);
 
 /*

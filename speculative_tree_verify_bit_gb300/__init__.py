@@ -28,6 +28,9 @@ STV_DEV_BAD_ROW = 4
 STV_DEV_BAD_COMMIT = 8
 STV_DEV_TIMEOUT = 16
 
+STV_KV_BY_GROUP = 0  # group 32: the 3-bit cache; group 256: the int4 per-token-head cache
+STV_KV_K4V2 = 2      # the K 4 / V 2-bit cache (group 32)
+
 STV_PATH_EXACT = 0
 STV_PATH_INT8 = 1
 PATHS = {"exact": STV_PATH_EXACT, "int8": STV_PATH_INT8}
@@ -57,7 +60,7 @@ class StvError(RuntimeError):
 
 class stv_shape(ctypes.Structure):
     _fields_ = [("hq", ctypes.c_int32), ("hkv", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("group", ctypes.c_int32), ("page_tokens", ctypes.c_int32)]
+                ("group", ctypes.c_int32), ("page_tokens", ctypes.c_int32), ("kv_format", ctypes.c_int32)]
 
 
 class stv_layer_cache(ctypes.Structure):
@@ -156,10 +159,11 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def make_shape(hq: int = 24, hkv: int = 4, group: int = GROUP) -> stv_shape:
+def make_shape(hq: int = 24, hkv: int = 4, group: int = GROUP, kv_format: int = STV_KV_BY_GROUP) -> stv_shape:
     """group 32: the 3-bit cache; group 256 (GROUP_INT4): the int4
-    per-token-head cache."""
-    return stv_shape(hq, hkv, HEAD_DIM, group, PAGE_TOKENS)
+    per-token-head cache; kv_format STV_KV_K4V2 (group 32): the K 4 / V 2-bit
+    cache (include/stv.h)."""
+    return stv_shape(hq, hkv, HEAD_DIM, group, PAGE_TOKENS, kv_format)
 
 
 def head_block_bytes(group: int = GROUP) -> int:

@@ -13,6 +13,8 @@ static int check_shape(const stv_shape* sh, int t_nodes, ShapeInfo* out) {
   if (!sh) return STV_ERR_INVALID_ARG;
   if (sh->head_dim != kHeadDim || sh->page_tokens != kPageTok) return STV_ERR_SHAPE_UNSUPPORTED;
   if (sh->group != kGroup && sh->group != kGroupI4) return STV_ERR_SHAPE_UNSUPPORTED;
+  if (sh->kv_format != STV_KV_BY_GROUP && !(sh->kv_format == STV_KV_K4V2 && sh->group == kGroup))
+    return STV_ERR_SHAPE_UNSUPPORTED;
   if (sh->hkv < 1 || sh->hq < sh->hkv || sh->hq % sh->hkv != 0) return STV_ERR_SHAPE_UNSUPPORTED;
   const int G = sh->hq / sh->hkv;
   if (t_nodes >= 0) {
@@ -25,14 +27,14 @@ static int check_shape(const stv_shape* sh, int t_nodes, ShapeInfo* out) {
     out->G = G;
     out->T = t_nodes;
     out->R = t_nodes * G;
-    out->i4 = sh->group == kGroupI4;
+    out->fmt = sh->kv_format == STV_KV_K4V2 ? kFmtK4V2 : (sh->group == kGroupI4 ? kFmtInt4 : kFmtBit3);
   }
   return STV_OK;
 }
 
 static int check_layer(const stv_layer_cache* l, const ShapeInfo& sh) {
   if (!l || !l->pool || l->n_pages < 1) return STV_ERR_INVALID_ARG;
-  if (l->page_bytes != (int64_t)sh.hkv * (sh.i4 ? kI4HeadBytes : kHeadBytes)) return STV_ERR_SHAPE_UNSUPPORTED;
+  if (l->page_bytes != (int64_t)sh.hkv * (sh.fmt == kFmtInt4 ? kI4HeadBytes : kHeadBytes)) return STV_ERR_SHAPE_UNSUPPORTED;
   return STV_OK;
 }
 
@@ -211,7 +213,7 @@ int stv_kv_append_pack(const stv_shape* shape, const stv_layer_cache* layer, con
   p.row_seq = row_seq;
   p.row_pos = row_pos;
   p.n_rows = n_rows;
-  p.i4 = sh.i4;
+  p.fmt = sh.fmt;
   p.status = dev_status;
   return to_status(launch_kv_append(p, (cudaStream_t)stream));
 }
@@ -240,7 +242,8 @@ static int verify_common(const stv_shape* shape, const stv_layer_cache* layer, c
   if (rc) return rc;
   if ((rc = check_layer(layer, sh)) || (rc = check_seqs(seqs, n_seqs, t_nodes))) return rc;
   if (!q || !parent || !workspace || (path != STV_PATH_EXACT && path != STV_PATH_INT8)) return STV_ERR_INVALID_ARG;
-  if (k_tree && sh.i4) return STV_ERR_UNIMPLEMENTED;  // the fused append packs the 3-bit cache only
+  if (k_tree && sh.fmt != kFmtBit3) return STV_ERR_UNIMPLEMENTED;  // the fused append packs the 3-bit cache only
+  if (path == STV_PATH_INT8 && sh.fmt == kFmtK4V2) return STV_ERR_UNIMPLEMENTED;  // exact path only on this cache
   int sm = 0;
   if ((rc = device_sm_count(&sm))) return rc;
   Plan plan;
@@ -271,7 +274,7 @@ static int verify_common(const stv_shape* shape, const stv_layer_cache* layer, c
   p.ml = reinterpret_cast<float*>(ws + wl.off_ml);
   p.k_tree = static_cast<const __half*>(k_tree);
   p.v_tree = static_cast<const __half*>(v_tree);
-  p.i4 = sh.i4;
+  p.fmt = sh.fmt;
   p.dots = dots;
   p.test_withhold_copies = withhold_copies;
   p.status = dev_status;
@@ -426,7 +429,7 @@ int stv_kv_commit(const stv_shape* shape, const stv_layer_cache* layers, int n_l
   p.n_commit = n_commit;
   p.path = path;
   p.ctx_dev = ctx_dev;
-  p.i4 = sh.i4;
+  p.fmt = sh.fmt;
   p.status = dev_status;
   return to_status(launch_kv_commit(p, (cudaStream_t)stream));
 }
@@ -437,7 +440,7 @@ int stv_int8_qk_dots(const stv_shape* shape, const stv_layer_cache* layer, const
   ShapeInfo sh;
   int rc = check_shape(shape, t_nodes, &sh);
   if (rc) return rc;
-  if (sh.i4) return STV_ERR_UNIMPLEMENTED;  // the per-group dots belong to the 3-bit cache
+  if (sh.fmt != kFmtBit3) return STV_ERR_UNIMPLEMENTED;  // the per-group dots belong to the 3-bit cache
   if (!dots) return STV_ERR_INVALID_ARG;
   return verify_common(shape, layer, seq, 1, nullptr, nullptr, q, parent, t_nodes, STV_PATH_INT8, workspace, ws_bytes,
                        dev_status, stream, dots);

@@ -88,10 +88,59 @@ __global__ void __launch_bounds__(256) kv_append_i4_kernel(const __grid_constant
   }
 }
 
+// The K 4 / V 2-bit cache (include/stv.h, STV_KV_K4V2): one CTA per (row, KV
+// head), thread = channel, warp = 32-channel group.  The 3-bit quantizer at
+// 4 bits (K: s = fp16(max / 8), codes -8..7) and 2 bits (V: s = fp16(max /
+// 2), codes -2..1); max / 8 and max / 2 are exact in fp32, so rounding them
+// to fp16 is fp16(max / h).  The division-free exact rounding of
+// rne_quotient gives the codes.  K: a word holds 8 channels, OR-reduced over
+// 8 lanes.  V: a word holds one channel's codes for 16 tokens; rows appended
+// in the same launch may share it (their bits differ), so it is updated
+// with atomics.
+__global__ void __launch_bounds__(256) kv_append_k4v2_kernel(const __grid_constant__ AppendParams p) {
+  const int row = blockIdx.x / p.hkv, h = blockIdx.x % p.hkv;
+  const int c = threadIdx.x, lane = c & 31, g = c >> 5;
+  const int s = __ldg(p.row_seq + row), pos = __ldg(p.row_pos + row);
+  if (s < 0 || s >= p.n_seqs || pos < 0) {
+    if (c == 0) report(p.status, STV_DEV_BAD_ROW);
+    return;
+  }
+  uint8_t* hb = const_cast<uint8_t*>(
+      head_block(p.seq[s], p.pool, p.page_bytes, p.pool_pages, pos, h, c == 0 ? p.status : nullptr, kKv2HeadBytes));
+  if (!hb) return;
+  const int slot = pos & (kPageTok - 1);
+  const int64_t src = ((int64_t)row * p.hkv + h) * kHeadDim + c;
+  const float xk = __half2float(p.k[src]), xv = __half2float(p.v[src]);
+  // K, 4 bits
+  const __half sk = __float2half_rn(warp_max(fabsf(xk)) * 0.125f);
+  const float skf = __half2float(sk);
+  const int uk = (skf == 0.f ? 0 : min(max(rne_quotient(xk, skf), -8), 7)) + 8;
+  uint32_t kw = (uint32_t)uk << i4_pos(lane & 7);
+  kw |= __shfl_xor_sync(0xffffffffu, kw, 1);
+  kw |= __shfl_xor_sync(0xffffffffu, kw, 2);
+  kw |= __shfl_xor_sync(0xffffffffu, kw, 4);
+  if ((lane & 7) == 0)
+    *reinterpret_cast<uint32_t*>(hb + kKv2OffKCodes + slot * 128 + g * 16 + (lane >> 3) * 4) = kw;
+  if (lane == 0) *reinterpret_cast<__half*>(hb + kKv2OffKScales + slot * 16 + g * 2) = sk;
+  // V, 2 bits
+  const __half sv = __float2half_rn(warp_max(fabsf(xv)) * 0.5f);
+  const float svf = __half2float(sv);
+  const uint32_t uv = (uint32_t)((svf == 0.f ? 0 : min(max(rne_quotient(xv, svf), -2), 1)) + 2);
+  const int tile = slot / kTileTok, within = slot % kTileTok;
+  if (lane == 0)
+    *reinterpret_cast<__half*>(hb + kKv2OffVScales + tile * kKv2VTileScaleBytes + g * (kTileTok * 2) + within * 2) = sv;
+  uint32_t* wp = reinterpret_cast<uint32_t*>(hb + kKv2OffVCodes + tile * kKv2VTileCodeBytes + c * 16 + (within / 16) * 4);
+  const int sh = v2_pos(within & 15);
+  atomicAnd(wp, ~(3u << sh));
+  atomicOr(wp, uv << sh);
+}
+
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t s) {
   if (p.n_rows == 0) return cudaSuccess;
-  if (p.i4)
+  if (p.fmt == kFmtInt4)
     kv_append_i4_kernel<<<p.n_rows * p.hkv, 256, 0, s>>>(p);
+  else if (p.fmt == kFmtK4V2)
+    kv_append_k4v2_kernel<<<p.n_rows * p.hkv, 256, 0, s>>>(p);
   else
     kv_append_kernel<<<p.n_rows * p.hkv, 256, 0, s>>>(p);
   return cudaGetLastError();
@@ -283,11 +332,95 @@ __global__ void __launch_bounds__(256) kv_commit_i4_kernel(const __grid_constant
   if (leader && p.ctx_dev) p.ctx_dev[s] += n;
 }
 
+// kv_commit for the K 4 / V 2-bit cache: the same protocol (validate the
+// path and every page, read every source row, then write), moving each row's
+// K codes and both scale rows whole and its V code channel by channel.
+__global__ void __launch_bounds__(256) kv_commit_k4v2_kernel(const __grid_constant__ CommitParams p) {
+  int b = blockIdx.x;
+  const int h = b % p.hkv;
+  b /= p.hkv;
+  const int layer = b % p.n_layers;
+  const int s = b / p.n_layers;
+  const int tid = threadIdx.x;
+  const bool leader = (layer == 0 && h == 0 && tid == 0);
+
+  __shared__ int path_s[kMaxT];
+  __shared__ int n_s, ok_s;
+  __shared__ __align__(16) uint8_t krow[kMaxT][144];  // 128 B codes + 16 B scales
+  __shared__ __align__(4) __half vscale[kMaxT][kGroups];
+  __shared__ uint8_t vcode[kMaxT][kHeadDim];
+
+  if (tid == 0) {
+    int n = __ldg(p.n_commit + s);
+    int ok = (n >= 1 && n <= p.T);
+    int prev = -1;
+    for (int i = 0; ok && i < n; ++i) {
+      int x = __ldg(p.path + (int64_t)s * p.T + i);
+      path_s[i] = x;
+      if ((i == 0 && x != 0) || x <= prev || x >= p.T) ok = 0;
+      prev = x;
+    }
+    n_s = n;
+    ok_s = ok ? (commit_pages_ok(p.seq[s], path_s, n, p.min_pool_pages) ? 1 : 2) : 0;
+  }
+  __syncthreads();
+  if (ok_s != 1) {
+    if (leader) report(p.status, ok_s == 0 ? STV_DEV_BAD_COMMIT : STV_DEV_BAD_PAGE);
+    return;
+  }
+  const int n = n_s;
+  const SeqDesc& sd = p.seq[s];
+  const uint8_t* pool = p.pools[layer];
+  const int32_t pool_pages = p.pool_pages[layer];
+
+  for (int i = 0; i < n; ++i) {
+    const int64_t src = (int64_t)sd.ctx + path_s[i];
+    const uint8_t* hb = head_block(sd, pool, p.page_bytes, pool_pages, src, h, nullptr, kKv2HeadBytes);  // validated
+    const int slot = (int)(src & (kPageTok - 1)), tile = slot / kTileTok, within = slot % kTileTok;
+    if (tid < 8)
+      reinterpret_cast<uint4*>(krow[i])[tid] = reinterpret_cast<const uint4*>(hb + kKv2OffKCodes + slot * 128)[tid];
+    else if (tid == 8)
+      reinterpret_cast<uint4*>(krow[i])[8] = *reinterpret_cast<const uint4*>(hb + kKv2OffKScales + slot * 16);
+    else if (tid >= 16 && tid < 24) {
+      const int g = tid - 16;
+      vscale[i][g] = *reinterpret_cast<const __half*>(hb + kKv2OffVScales + tile * kKv2VTileScaleBytes +
+                                                      g * (kTileTok * 2) + within * 2);
+    }
+    const uint32_t w =
+        *reinterpret_cast<const uint32_t*>(hb + kKv2OffVCodes + tile * kKv2VTileCodeBytes + tid * 16 + (within / 16) * 4);
+    vcode[i][tid] = (uint8_t)((w >> v2_pos(within & 15)) & 3u);
+  }
+  __syncthreads();
+
+  for (int i = 0; i < n; ++i) {
+    const int64_t dst = (int64_t)sd.ctx + i;
+    uint8_t* hb = const_cast<uint8_t*>(head_block(sd, pool, p.page_bytes, pool_pages, dst, h, nullptr, kKv2HeadBytes));
+    const int slot = (int)(dst & (kPageTok - 1)), tile = slot / kTileTok, within = slot % kTileTok;
+    if (tid < 8)
+      reinterpret_cast<uint4*>(hb + kKv2OffKCodes + slot * 128)[tid] = reinterpret_cast<const uint4*>(krow[i])[tid];
+    else if (tid == 8)
+      *reinterpret_cast<uint4*>(hb + kKv2OffKScales + slot * 16) = reinterpret_cast<const uint4*>(krow[i])[8];
+    else if (tid >= 16 && tid < 24) {
+      const int g = tid - 16;
+      *reinterpret_cast<__half*>(hb + kKv2OffVScales + tile * kKv2VTileScaleBytes + g * (kTileTok * 2) + within * 2) =
+          vscale[i][g];
+    }
+    // Channel `tid` owns its V words in this head: plain read-modify-write.
+    uint32_t* wp = reinterpret_cast<uint32_t*>(hb + kKv2OffVCodes + tile * kKv2VTileCodeBytes + tid * 16 + (within / 16) * 4);
+    const int sh = v2_pos(within & 15);
+    *wp = (*wp & ~(3u << sh)) | ((uint32_t)vcode[i][tid] << sh);
+  }
+  if (leader && p.ctx_dev) p.ctx_dev[s] += n;
+}
+
 cudaError_t launch_kv_commit(const CommitParams& p, cudaStream_t s) {
-  if (p.i4)
-    kv_commit_i4_kernel<<<p.n_seqs * p.n_layers * p.hkv, 256, 0, s>>>(p);
+  const int blocks = p.n_seqs * p.n_layers * p.hkv;
+  if (p.fmt == kFmtInt4)
+    kv_commit_i4_kernel<<<blocks, 256, 0, s>>>(p);
+  else if (p.fmt == kFmtK4V2)
+    kv_commit_k4v2_kernel<<<blocks, 256, 0, s>>>(p);
   else
-    kv_commit_kernel<<<p.n_seqs * p.n_layers * p.hkv, 256, 0, s>>>(p);
+    kv_commit_kernel<<<blocks, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

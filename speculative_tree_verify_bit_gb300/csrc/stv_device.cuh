@@ -144,6 +144,38 @@ __device__ __forceinline__ int quant_code_i4(float x, float s) {
 // for odd e, so that one AND/OR per pair makes an fp16 pair (below).
 __device__ __forceinline__ int i4_pos(int e) { return ((e & 1) ? 16 : 0) + 4 * (e >> 1); }
 
+// Bit position of token t (0..15) in a 2-bit V word of the K 4 / V 2-bit
+// cache: 2 * (t / 2), plus 16 for odd t, so that one AND/OR per pair makes
+// an fp16 pair (decode_v2_block_h2).
+__device__ __forceinline__ int v2_pos(int t) { return ((t & 1) ? 16 : 0) + 2 * (t >> 1); }
+
+// Decode one channel's 2-bit V codes for 32 tokens (two words; pairs (2m,
+// 2m+1) in order) into 16 fp16 pairs scale * (u - 2).  The pair at bits
+// 2k, 16 + 2k (k = 0..3 of each byte-pair) drops into the mantissas of 1024,
+// 256, 64 or 16 (lowest field bit weighing 1) with one AND/OR, giving
+// base + u exactly; subtracting base + 2 is exact; the product with the
+// scale pair is one fp16 rounding.
+template <typename ScaleFn>
+__device__ __forceinline__ void decode_v2_block_h2(uint32_t w0, uint32_t w1, ScaleFn scale, __half2 (&out)[16]) {
+  const __half2 b1026 = u32_as_h2(0x64026402u);  // 1026
+  const __half2 b258 = u32_as_h2(0x5C085C08u);   // 258
+  const __half2 b66 = u32_as_h2(0x54205420u);    // 66
+  const __half2 b18 = u32_as_h2(0x4C804C80u);    // 18
+  const uint32_t w[2] = {w0, w1};
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const uint32_t x = half ? (w[j] >> 8) : w[j];
+      const int m = 8 * j + 4 * half;
+      out[m + 0] = __hmul2(__hsub2(u32_as_h2((x & 0x00030003u) | 0x64006400u), b1026), scale(m + 0));
+      out[m + 1] = __hmul2(__hsub2(u32_as_h2((x & 0x000C000Cu) | 0x5C005C00u), b258), scale(m + 1));
+      out[m + 2] = __hmul2(__hsub2(u32_as_h2((x & 0x00300030u) | 0x54005400u), b66), scale(m + 2));
+      out[m + 3] = __hmul2(__hsub2(u32_as_h2((x & 0x00C000C0u) | 0x4C004C00u), b18), scale(m + 3));
+    }
+  }
+}
+
 // Decode four int4 words (32 elements, pairs (2m, 2m+1) in order) into 16
 // fp16 pairs of the signed codes c = u - 8.  Elements 0/1 of a word drop into
 // the mantissas of 1024 (lowest bit weighs 1) and elements 2/3 into those of

@@ -45,6 +45,19 @@ constexpr int kI4VTileCodeBytes = kHeadDim * 32;              // 8192
 constexpr int kI4VTileScaleBytes = kTileTok * 2;              // 128
 static_assert(kI4HeadBytes == STV_HEAD_BLOCK_BYTES_INT4, "layout");
 
+// The K 4 / V 2-bit format (group 32; see include/stv.h).
+constexpr int kKv2OffKCodes = 0;
+constexpr int kKv2OffKScales = kPageTok * kGroups * 16;                 // 32768
+constexpr int kKv2OffVCodes = kKv2OffKScales + kPageTok * kGroups * 2;  // 36864
+constexpr int kKv2OffVScales = kKv2OffVCodes + kPageTok * kHeadDim / 4;  // 53248
+constexpr int kKv2HeadBytes = kKv2OffVScales + kPageTok * kGroups * 2;  // 57344
+constexpr int kKv2KTileCodeBytes = kTileTok * 128;                      // 8192: one 64-token tile
+constexpr int kKv2KTileScaleBytes = kTileTok * 16;                      // 1024
+constexpr int kKv2VTileCodeBytes = kHeadDim * 16;                       // 4096
+constexpr int kKv2VTileScaleBytes = kGroups * kTileTok * 2;             // 1024
+static_assert(kKv2HeadBytes == STV_HEAD_BLOCK_BYTES, "layout");
+static_assert(kKv2OffVScales == kOffVScales, "V scales sit where the 3-bit cache's do");
+
 struct SeqDesc {
   const int32_t* page_table;
   int32_t n_pages;
@@ -68,9 +81,13 @@ struct WsLayout {
   size_t off_qi, off_sq, off_opart, off_ml, total;
 };
 
+// Cache formats (include/stv.h): the pages' 3-bit cache, the int4
+// per-token-head cache, the K 4 / V 2-bit cache.
+enum { kFmtBit3 = 0, kFmtInt4 = 1, kFmtK4V2 = 2 };
+
 struct ShapeInfo {
   int hq, hkv, G, T, R;  // R = T * G rows per KV head
-  int i4;                // 1: the int4 per-token-head cache (group 256)
+  int fmt;               // kFmtBit3, kFmtInt4 or kFmtK4V2
 };
 
 // Parameters of one verify launch (passed by value; < 4 KB).
@@ -95,7 +112,7 @@ struct VerifyParams {
   // sequence s goes to position ctx_s + i.
   const __half* k_tree;
   const __half* v_tree;
-  int i4;  // int4 per-token-head cache
+  int fmt;  // cache format
   // Inspection (int8 path, one sequence): when set, the verify kernel also
   // writes its own per-group integer dots, int32 [hkv][R][ctx + T][8].
   int32_t* dots;
@@ -126,7 +143,7 @@ struct AppendParams {
   const int32_t* row_seq;
   const int32_t* row_pos;
   int n_rows;
-  int i4;  // int4 per-token-head cache
+  int fmt;  // cache format
   int32_t* status;
 };
 
@@ -141,7 +158,7 @@ struct CommitParams {
   const int32_t* n_commit;
   const int32_t* path;
   int32_t* ctx_dev;
-  int i4;  // int4 per-token-head cache
+  int fmt;  // cache format
   int32_t* status;
 };
 

@@ -58,8 +58,8 @@ constexpr int kSmemBytes = 1024 /*align slack*/ + (2 + kVBuffers) * kOperandByte
 // issues only after the softmax of tile i has arrived on p_full, so a slot is
 // never rewritten while it is read.
 constexpr int kKScaleSlots = 4;
-template <bool kI4>
-struct Fmt {
+template <int kFmt>
+struct Fmt {  // the 3-bit cache
   static constexpr int stages = kStages;
   static constexpr int head = kHeadBytes;
   static constexpr int off_kc = kOffKCodes, off_ks = kOffKScales, off_vc = kOffVCodes, off_vs = kOffVScales;
@@ -68,7 +68,7 @@ struct Fmt {
   static constexpr int smem = kSmemBytes;
 };
 template <>
-struct Fmt<true> {
+struct Fmt<kFmtInt4> {
   static constexpr int stages = 3;
   static constexpr int head = kI4HeadBytes;
   static constexpr int off_kc = kI4OffKCodes, off_ks = kI4OffKScales, off_vc = kI4OffVCodes, off_vs = kI4OffVScales;
@@ -77,8 +77,21 @@ struct Fmt<true> {
   // + the per-key K scales of the last kKScaleSlots tiles, as fp32
   static constexpr int smem = 1024 + (2 + kVBuffers) * kOperandBytes + stages * stage + 1024 + kKScaleSlots * kTileTok * 4;
 };
-static_assert(Fmt<true>::stages <= kStages, "barrier arrays");
-static_assert(Fmt<true>::smem <= 232448, "shared memory per CTA");
+// The K 4 / V 2-bit cache: a tile's arrays take the 3-bit cache's 14,336 bytes.
+template <>
+struct Fmt<kFmtK4V2> {
+  static constexpr int stages = kStages;
+  static constexpr int head = kKv2HeadBytes;
+  static constexpr int off_kc = kKv2OffKCodes, off_ks = kKv2OffKScales, off_vc = kKv2OffVCodes,
+                       off_vs = kKv2OffVScales;
+  static constexpr int kc = kKv2KTileCodeBytes, ks = kKv2KTileScaleBytes, vc = kKv2VTileCodeBytes,
+                       vs = kKv2VTileScaleBytes;
+  static constexpr int stage = kc + ks + vc + vs;  // 14336
+  static constexpr int smem = kSmemBytes;
+};
+static_assert(Fmt<kFmtK4V2>::stage == kStageBytes, "stage");
+static_assert(Fmt<kFmtInt4>::stages <= kStages, "barrier arrays");
+static_assert(Fmt<kFmtInt4>::smem <= 232448, "shared memory per CTA");
 constexpr float kRescaleThreshold = 8.f;  // log2 units
 
 constexpr uint32_t kColQ = 0, kColS0 = 128, kColO = 256, kTmemCols = 512;
@@ -115,9 +128,11 @@ __device__ __forceinline__ bool settle(uint64_t* b, uint32_t parity, uint32_t pr
 // (stv_append_verify_attn); the plain instantiation carries none of that code.
 // kWithhold (failure-path test only, stv_verify_attn_timeout_test): the
 // producer issues no copy, so every wait on one runs out.
-template <bool kAppend, bool kI4, bool kWithhold = false>
+template <bool kAppend, int kFmt, bool kWithhold = false>
 __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_constant__ VerifyParams p) {
-  using F = Fmt<kI4>;
+  using F = Fmt<kFmt>;
+  constexpr bool kI4 = kFmt == kFmtInt4;    // one K scale per key, handed to the softmax
+  constexpr bool kKv2 = kFmt == kFmtK4V2;  // 4-bit K, 2-bit V, scales per 32-channel group
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment of the operand tiles (the swizzle works on address bits).
   const uint32_t base_u32 = su32(smem_raw);
@@ -467,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
     // mod 4) and start at different halves (j mod 2), which makes the loads
     // conflict-free while the stores keep 8 different keys per group.
     const int kj = (ut >> 5) * 8 + (ut & 7);
-    const int kcb = kI4 ? (((ut & 7) >> 1) + ((ut >> 3) & 3)) & 3 : (ut >> 3) & 3;
+    const int kcb = (kI4 || kKv2) ? (((ut & 7) >> 1) + ((ut >> 3) & 3)) & 3 : (ut >> 3) & 3;
     const int vch = ut;  // V: channel
     // ---- fused append: the tree rows whose keys fall in this unit's range ----
     // (a1 for KV head h; thread ut = channel, warp = 32-channel group, the
@@ -578,6 +593,27 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
           st_shared_v4(sw128_chunk(krow, 4 + q4), out[4 * q4], out[4 * q4 + 1], out[4 * q4 + 2], out[4 * q4 + 3]);
+      } else if constexpr (kKv2) {
+        // 4-bit K: key kj's groups 2 kcb and 2 kcb + 1 are 4 words each (a
+        // key's codes are one 128-byte row: the int4 lane mapping keeps the
+        // loads conflict-free), times their group scales
+        const uint4* wq = reinterpret_cast<const uint4*>(stage + kj * 128 + kcb * 32);
+        const int hf = kj & 1;
+        const uint4 x0 = wq[hf], x1 = wq[hf ^ 1];
+        const uint4 a0 = hf ? x1 : x0, a1 = hf ? x0 : x1;
+        const __half2 sc2 = *reinterpret_cast<const __half2*>(stage + F::kc + kj * 16 + kcb * 4);
+        const __half2 s0 = __low2half2(sc2), s1 = __high2half2(sc2);
+        const uint32_t krow = su32(kdeq0) + b * kOperandBytes + kcb * 8192 + sw128_row(kj);
+        __half2 out[16];
+        const uint32_t w0[4] = {a0.x, a0.y, a0.z, a0.w}, w1[4] = {a1.x, a1.y, a1.z, a1.w};
+        decode_i4_block_h2(w0, [&](int) { return s0; }, out);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          st_shared_v4(sw128_chunk(krow, q4), out[4 * q4], out[4 * q4 + 1], out[4 * q4 + 2], out[4 * q4 + 3]);
+        decode_i4_block_h2(w1, [&](int) { return s1; }, out);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          st_shared_v4(sw128_chunk(krow, 4 + q4), out[4 * q4], out[4 * q4 + 1], out[4 * q4 + 2], out[4 * q4 + 3]);
       } else {
         const uint2* wv = reinterpret_cast<const uint2*>(stage + kj * 96 + kcb * 24);
         const uint2 w01 = wv[0], w23 = wv[1], w45 = wv[2];
@@ -633,11 +669,20 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
             st_shared_v4(sw128_chunk(vrow, blk * 4 + q4), out[4 * q4], out[4 * q4 + 1], out[4 * q4 + 2], out[4 * q4 + 3]);
         }
       } else {
-        const uint2* wv = reinterpret_cast<const uint2*>(stage + kKTileCodeBytes + kKTileScaleBytes + vch * 24);
-        const uint2 w01 = wv[0], w23 = wv[1], w45 = wv[2];
+        // 3-bit V: channel vch's 64 keys are 2 blocks of 3 words; 2-bit V
+        // (K 4 / V 2 cache): 4 words of 16 keys
+        uint32_t vw[6];
+        if constexpr (kKv2) {
+          const uint4 x = *reinterpret_cast<const uint4*>(stage + F::kc + F::ks + vch * 16);
+          vw[0] = x.x; vw[1] = x.y; vw[2] = x.z; vw[3] = x.w; vw[4] = vw[5] = 0u;
+        } else {
+          const uint2* wv = reinterpret_cast<const uint2*>(stage + F::kc + F::ks + vch * 24);
+          const uint2 w01 = wv[0], w23 = wv[1], w45 = wv[2];
+          vw[0] = w01.x; vw[1] = w01.y; vw[2] = w23.x; vw[3] = w23.y; vw[4] = w45.x; vw[5] = w45.y;
+        }
         // this channel's group: 64 key scales, as 32 (key 2m, 2m+1) pairs
-        const uint4* sp = reinterpret_cast<const uint4*>(stage + kKTileCodeBytes + kKTileScaleBytes +
-                                                         kVTileCodeBytes + (vch >> 5) * (kTileTok * 2));
+        const uint4* sp =
+            reinterpret_cast<const uint4*>(stage + F::kc + F::ks + F::vc + (vch >> 5) * (kTileTok * 2));
         const int live = tok1 - key0;  // keys at or beyond this are zeroed
         const uint32_t vrow = su32(vdeq0) + vb * kOperandBytes + sw128_row(vch);
 #pragma unroll
@@ -652,10 +697,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
             sc[4 * q + 3] = x.w;
           }
           __half2 out[16];
-          if (blk == 0)
-            decode_block_h2(w01.x, w01.y, w23.x, [&](int m) { return u32_as_h2(sc[m]); }, out);
+          if constexpr (kKv2)
+            decode_v2_block_h2(vw[2 * blk], vw[2 * blk + 1], [&](int m) { return u32_as_h2(sc[m]); }, out);
           else
-            decode_block_h2(w23.y, w45.x, w45.y, [&](int m) { return u32_as_h2(sc[m]); }, out);
+            decode_block_h2(vw[3 * blk], vw[3 * blk + 1], vw[3 * blk + 2], [&](int m) { return u32_as_h2(sc[m]); }, out);
           if (live < 64) {
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
@@ -689,21 +734,28 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
   if (tid == 0 && bars->abort) report(p.status, STV_DEV_TIMEOUT);
 }
 
-}  // namespace
-
-cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s) {
-  // the int8 path on the 3-bit cache forms per-group integer dots: its own kernel
-  if (p.path == STV_PATH_INT8 && !p.i4) return launch_verify_i8(p, s);
-  const bool append = p.k_tree != nullptr && p.v_tree != nullptr;
-  // the fused append packs the 3-bit cache only (the host refuses it for int4)
-  auto kernel = p.test_withhold_copies ? (p.i4 ? verify_tc_kernel<false, true, true> : verify_tc_kernel<false, false, true>)
-                : p.i4 ? verify_tc_kernel<false, true>
-                       : (append ? verify_tc_kernel<true, false> : verify_tc_kernel<false, false>);
-  const int smem = p.i4 ? Fmt<true>::smem : Fmt<false>::smem;
+template <bool kAppend, int kFmt, bool kWithhold = false>
+cudaError_t launch_one(const VerifyParams& p, cudaStream_t s) {
+  auto kernel = verify_tc_kernel<kAppend, kFmt, kWithhold>;
+  constexpr int smem = Fmt<kFmt>::smem;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kernel<<<p.n_units, kThreads, smem, s>>>(p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s) {
+  // the int8 path on the 3-bit cache forms per-group integer dots: its own kernel
+  if (p.path == STV_PATH_INT8 && p.fmt == kFmtBit3) return launch_verify_i8(p, s);
+  if (p.test_withhold_copies)
+    return p.fmt == kFmtInt4 ? launch_one<false, kFmtInt4, true>(p, s) : launch_one<false, kFmtBit3, true>(p, s);
+  // the fused append packs the 3-bit cache only (the host refuses it for the others)
+  const bool append = p.k_tree != nullptr && p.v_tree != nullptr;
+  if (p.fmt == kFmtInt4) return launch_one<false, kFmtInt4>(p, s);
+  if (p.fmt == kFmtK4V2) return launch_one<false, kFmtK4V2>(p, s);
+  return append ? launch_one<true, kFmtBit3>(p, s) : launch_one<false, kFmtBit3>(p, s);
 }
 
 }  // namespace stv

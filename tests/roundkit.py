@@ -20,7 +20,7 @@ class Round:
     """Inputs of one layer's round: contexts, trees, fp16 K/V/Q, page tables."""
 
     def __init__(self, ctx, t_nodes, seed, hq=24, hkv=4, tree="random", p_accept=0.7, max_depth=8,
-                 device="cuda", extra_pages=1, parents=None, group=32):
+                 device="cuda", extra_pages=1, parents=None, group=32, kind=None):
         self.ctx = list(ctx)
         self.n_seqs = len(self.ctx)
         self.T, self.hq, self.hkv = t_nodes, hq, hkv
@@ -61,7 +61,8 @@ class Round:
         self.row_pos = np.concatenate([np.arange(c + t_nodes, dtype=np.int32) for c in self.ctx])
         self.q = workloads.q_rows(seed, self.n_seqs, t_nodes, hq, device=device).contiguous()
         self.group = group  # 32: the 3-bit cache; 256: the int4 per-token-head cache
-        self.shape = stv.make_shape(hq, hkv, group)
+        self.kind = kind    # "k4v2": the K 4 / V 2-bit cache (group 32)
+        self.shape = stv.make_shape(hq, hkv, group, stv.STV_KV_K4V2 if kind == "k4v2" else stv.STV_KV_BY_GROUP)
 
     # ---------------- GPU side ----------------
     def gpu_cache(self):
@@ -91,7 +92,7 @@ class Round:
 
     # ---------------- oracle side ----------------
     def oracle_cache(self):
-        cache = oracle.Cache(self.hkv, self.pool_pages, bits=4 if self.group == 256 else 3)
+        cache = oracle.Cache(self.hkv, self.pool_pages, bits=4 if self.group == 256 else 3, kind=self.kind)
         oracle.kv_append(cache, self.tables, self.k.cpu().numpy(), self.v.cpu().numpy(), self.row_seq, self.row_pos)
         self.ocache = cache
         return cache
