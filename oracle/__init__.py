@@ -38,16 +38,60 @@ HEAD_BYTES_I4 = 66560  # int4 per token and head (next row f3)
 FORMATS = {"bit3": 0, "int4": 1, "k4v2": 2}  # cache formats (stv_oracle.c): 3-bit; int4 per token-head; K 4 / V 2 bits
 
 
+def compile_c(src: str, out: str) -> None:
+    """gcc, -O2, portable C11 (no flag that changes float semantics)."""
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", out, src, "-lm", "-lpthread"])
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle into ``oracle/liboracle.so`` (gcc, -O2, portable)."""
+    """Compile the oracle into ``oracle/liboracle.so``."""
     stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
     if force or stale:
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(
-            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm", "-lpthread"]
-        )
+        compile_c(_SRC, tmp)
         os.replace(tmp, _LIB)
     return _LIB
+
+
+def bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Declare the argument and result types of the oracle's C functions on a
+    loaded library (the oracle's own build, or a test's copy of it)."""
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    I32 = ctypes.c_int32
+    I64 = ctypes.c_int64
+    lib.orc_half_to_double.restype = ctypes.c_double
+    lib.orc_half_to_double.argtypes = [ctypes.c_uint16]
+    lib.orc_double_to_half.restype = ctypes.c_uint16
+    lib.orc_double_to_half.argtypes = [ctypes.c_double]
+    lib.orc_quantize_group.argtypes = [P, P, P]
+    lib.orc_pack_block.argtypes = [P, P]
+    lib.orc_block_code.restype = ctypes.c_uint8
+    lib.orc_block_code.argtypes = [P, I]
+    lib.orc_kv_append.restype = I
+    lib.orc_kv_append.argtypes = [P, I64, I32, I32, P, P, I, P, P, P, P, I, I]
+    lib.orc_check_tree.restype = I
+    lib.orc_check_tree.argtypes = [P, I]
+    lib.orc_ancestors.restype = I
+    lib.orc_ancestors.argtypes = [P, I, P]
+    lib.orc_quantize_q_int8.argtypes = [P, P, P]
+    lib.orc_attention.restype = I
+    lib.orc_attention.argtypes = [P, I64, I32, I32, I32, P, P, P, I, P, P, I, I, P, I, P, I, I]
+    lib.orc_int8_dots.restype = I
+    lib.orc_int8_dots.argtypes = [P, I64, I32, I32, I32, P, P, I, P, I, I64, I64, P, I]
+    lib.orc_tree_accept.restype = I
+    lib.orc_tree_accept.argtypes = [P, P, P, I, P, P, P]
+    lib.orc_kv_commit.restype = I
+    lib.orc_kv_commit.argtypes = [P, I64, I32, I32, P, P, P, I, P, P, I, I]
+    lib.orc_decode_rows.restype = I
+    lib.orc_decode_rows.argtypes = [P, I64, I32, I32, P, P, I, I64, I64, I, P, I]
+    lib.orc_quantize_row_i4.restype = None
+    lib.orc_quantize_row_i4.argtypes = [P, P, P]
+    lib.orc_quantize_group_bits.restype = None
+    lib.orc_quantize_group_bits.argtypes = [P, I, P, P]
+    lib.orc_lookup_draft.restype = I
+    lib.orc_lookup_draft.argtypes = [P, I64, I, I, I, P, P, P, P]
+    return lib
 
 
 def _load():
@@ -55,43 +99,7 @@ def _load():
     with _lock:
         if _lib is None:
             build()
-            lib = ctypes.CDLL(_LIB)
-            P = ctypes.c_void_p
-            I = ctypes.c_int
-            I32 = ctypes.c_int32
-            I64 = ctypes.c_int64
-            lib.orc_half_to_double.restype = ctypes.c_double
-            lib.orc_half_to_double.argtypes = [ctypes.c_uint16]
-            lib.orc_double_to_half.restype = ctypes.c_uint16
-            lib.orc_double_to_half.argtypes = [ctypes.c_double]
-            lib.orc_quantize_group.argtypes = [P, P, P]
-            lib.orc_pack_block.argtypes = [P, P]
-            lib.orc_block_code.restype = ctypes.c_uint8
-            lib.orc_block_code.argtypes = [P, I]
-            lib.orc_kv_append.restype = I
-            lib.orc_kv_append.argtypes = [P, I64, I32, I32, P, P, I, P, P, P, P, I, I]
-            lib.orc_check_tree.restype = I
-            lib.orc_check_tree.argtypes = [P, I]
-            lib.orc_ancestors.restype = I
-            lib.orc_ancestors.argtypes = [P, I, P]
-            lib.orc_quantize_q_int8.argtypes = [P, P, P]
-            lib.orc_attention.restype = I
-            lib.orc_attention.argtypes = [P, I64, I32, I32, I32, P, P, P, I, P, P, I, I, P, I, P, I, I]
-            lib.orc_int8_dots.restype = I
-            lib.orc_int8_dots.argtypes = [P, I64, I32, I32, I32, P, P, I, P, I, I64, I64, P, I]
-            lib.orc_tree_accept.restype = I
-            lib.orc_tree_accept.argtypes = [P, P, P, I, P, P, P]
-            lib.orc_kv_commit.restype = I
-            lib.orc_kv_commit.argtypes = [P, I64, I32, I32, P, P, P, I, P, P, I, I]
-            lib.orc_decode_rows.restype = I
-            lib.orc_decode_rows.argtypes = [P, I64, I32, I32, P, P, I, I64, I64, I, P, I]
-            lib.orc_quantize_row_i4.restype = None
-            lib.orc_quantize_row_i4.argtypes = [P, P, P]
-            lib.orc_quantize_group_bits.restype = None
-            lib.orc_quantize_group_bits.argtypes = [P, I, P, P]
-            lib.orc_lookup_draft.restype = I
-            lib.orc_lookup_draft.argtypes = [P, I64, I, I, I, P, P, P, P]
-            _lib = lib
+            _lib = bind(ctypes.CDLL(_LIB))
     return _lib
 
 
