@@ -334,11 +334,14 @@ int stv_verify_attn_no_alloc(const stv_shape* shape, const stv_layer_cache* laye
  * prompt attends causally to the cache and to the prompt tokens before it.
  * "elpis" README, "Why fast" (prefill int8 Q.K^T, 3021c; prefill K/V
  * double-buffered ring, 3022: the next tile loads while the current one is
- * computed).  Built on the verify kernel: a chunk of C consecutive prompt
- * tokens is a chain tree (parent[i] = i - 1), whose ancestor-or-self mask is
- * the causal mask, appended after the tokens before it; C = min(32,
- * floor(128 / (hq / hkv))) rows per chunk fill the 128-row tile; up to 64
- * chunks run in one verify launch, then the split merge.
+ * computed).  A chunk of C consecutive prompt tokens is a chain tree
+ * (parent[i] = i - 1), whose ancestor-or-self mask is the causal mask,
+ * appended after the tokens before it; C = min(32, floor(128 / (hq / hkv)))
+ * rows per chunk fill the 128-row tile.  Exact path on the 3-bit cache: one
+ * persistent launch, one CTA per SM walking (chunk, KV head) units longest
+ * first, each over the chunk's whole key range, writing O / l directly (the
+ * workspace is not used).  int8 path and the other cache formats: up to 64
+ * chunks per verify launch, then the split merge.
  *  seq:      ctx = tokens cached before the prompt; the prompt's own K/V
  *            rows must already be in the cache at ctx .. ctx + n_tokens - 1
  *            (stv_kv_append_pack), so attention reads them in 3-bit, like

@@ -372,6 +372,34 @@ int stv_prefill_attn(const stv_shape* shape, const stv_layer_cache* layer, const
   if (!layer || !q || !o || !workspace) return STV_ERR_INVALID_ARG;
   if (ws_bytes < need) return STV_ERR_WORKSPACE_TOO_SMALL;
   const int c = prefill_chunk_tokens(shape);
+  ShapeInfo sh;
+  if ((rc = check_shape(shape, -1, &sh))) return rc;
+  if (path == STV_PATH_EXACT && sh.fmt == kFmtBit3) {
+    // one persistent launch over (chunk, KV head) units; no workspace used
+    if ((rc = check_layer(layer, sh))) return rc;
+    if ((rc = check_seqs(seq, 1, n_tokens))) return rc;
+    PrefillParams pp;
+    memset(&pp, 0, sizeof(pp));
+    pp.page_table = seq->page_table;
+    pp.n_pages = seq->n_pages;
+    pp.ctx0 = seq->ctx;
+    pp.n_tokens = n_tokens;
+    pp.chunk = c;
+    pp.n_chunks = (n_tokens + c - 1) / c;
+    pp.n_units = pp.n_chunks * sh.hkv;
+    pp.hq = sh.hq;
+    pp.hkv = sh.hkv;
+    pp.G = sh.G;
+    pp.pool = layer->pool;
+    pp.page_bytes = layer->page_bytes;
+    pp.pool_pages = layer->n_pages;
+    pp.q = static_cast<const __half*>(q);
+    pp.o = static_cast<__half*>(o);
+    pp.status = dev_status;
+    int sms = 0;
+    if ((rc = device_sm_count(&sms))) return rc;
+    return to_status(launch_prefill(pp, std::min(pp.n_units, sms), (cudaStream_t)stream));
+  }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* parents = reinterpret_cast<int32_t*>(ws);
   // chain parents for STV_MAX_SEQS chunks of c tokens; a last partial chunk

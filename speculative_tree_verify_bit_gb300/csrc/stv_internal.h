@@ -122,6 +122,24 @@ struct VerifyParams {
   int32_t* status;
 };
 
+// Parameters of one prefill launch (prefill_tc.cu, exact path, 3-bit cache):
+// the prompt of one sequence, cut into chunks of `chunk` tokens; a unit is
+// (chunk, KV head), numbered longest first.
+struct PrefillParams {
+  const int32_t* page_table;  // the sequence's pages
+  int32_t n_pages;
+  int32_t ctx0;      // cached tokens before the prompt
+  int n_tokens;      // prompt tokens, already in the cache at ctx0 ..
+  int chunk, n_chunks, n_units;
+  int hq, hkv, G;
+  const uint8_t* pool;
+  int64_t page_bytes;
+  int32_t pool_pages;
+  const __half* q;   // [n_tokens][hq][256]
+  __half* o;         // [n_tokens][hq][256]
+  int32_t* status;
+};
+
 struct CombineParams {
   SeqDesc seq[STV_MAX_SEQS];
   int n_seqs;
@@ -174,6 +192,7 @@ cudaError_t launch_quantize_q(const __half* q, int n_rows, int8_t* qi, float* sq
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);     // exact path; int4 cache (verify_tc.cu)
 cudaError_t launch_verify_i8(const VerifyParams& p, cudaStream_t s);  // int8 path, 3-bit cache (verify_i8.cu)
 cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillParams& p, int grid, cudaStream_t s);  // prefill_tc.cu
 cudaError_t launch_tree_accept(const int32_t* parent, const int32_t* draft, const int32_t* argmax, int T, int n_seqs,
                                int32_t* n_commit, int32_t* path, int32_t* out_ids, int32_t* status, cudaStream_t s);
 

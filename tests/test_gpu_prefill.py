@@ -6,7 +6,9 @@ The GPU splits the prompt into chain-tree chunks; the oracle side does not:
 each sampled prompt token t is its own one-node sequence whose context is
 ctx + t, so it sees exactly the cached tokens and the prompt tokens up to
 itself.  Sampled tokens include every chunk boundary region, the boundary
-between launches (64 chunks) and the ragged tail."""
+between launches of the chunked path (64 chunks), the ragged tail and the
+last chunks (the longest units, which the persistent exact-path kernel takes
+first)."""
 import numpy as np
 import pytest
 import torch
@@ -53,6 +55,7 @@ def sampled_tokens(n, c, rng):
         if b % (64 * c) == 0 or len(ts) < 24:
             ts.update({b - 1, b})
     ts.update(rng.integers(0, n, 8).tolist())
+    ts.update(range(max(0, n - 2 * c - 1), n, max(1, c // 3)))  # the last two chunks
     return sorted(t for t in ts if 0 <= t < n)
 
 
@@ -65,6 +68,21 @@ def sampled_tokens(n, c, rng):
     (5000, 500, 8, 4),      # G = 2: chunks of 32 tokens
 ])
 def test_prefill_matches_per_token_oracle(gpu, path, ctx0, n, hq, hkv):
+    check_prefill(path, ctx0, n, hq, hkv)
+
+
+@pytest.mark.parametrize("ctx0,n,hq,hkv", [
+    (700, 3000, 24, 4),     # 143 chunks x 4 heads = 572 units: several per CTA; tail of 18 tokens
+    (0, 2048, 32, 4),       # G = 8: chunks of 16 tokens, 128 rows
+    (64, 1100, 24, 1),      # one KV head, G = 24: chunks of 5 tokens (120 rows)
+    (255, 97, 8, 4),        # G = 2: three full chunks of 32 and one token
+])
+def test_prefill_persistent_exact_path(gpu, ctx0, n, hq, hkv):
+    """The exact path's persistent kernel over many (chunk, KV head) units."""
+    check_prefill("exact", ctx0, n, hq, hkv)
+
+
+def check_prefill(path, ctx0, n, hq, hkv):
     seed = 9100 + ctx0 + n + hq
     shape, layer, seq, q, table, cache = prefill_case(ctx0, n, hq, hkv, seed)
     got = gpu_prefill(shape, layer, seq, q, n, path)
@@ -79,6 +97,22 @@ def test_prefill_matches_per_token_oracle(gpu, path, ctx0, n, hq, hkv):
     want = np.asarray(want).reshape(len(heads), len(ts), 256)
     got_rows = np.stack([got[ts, h] for h in heads])
     assert_attention_close(got_rows, want, f"prefill ctx0={ctx0} n={n} {path}")
+
+
+def test_prefill_reports_bad_page(gpu):
+    """A page-table entry outside the pool: the kernel reads a valid page in
+    its place, finishes, and reports STV_DEV_BAD_PAGE."""
+    shape, layer, seq, q, table, cache = prefill_case(300, 200, 24, 4, 17)
+    bad = seq.page_table.clone()
+    bad[0] = layer.n_pages + 5
+    ws = torch.empty(stv.stv_prefill_workspace_bytes(shape, seq, 200), dtype=torch.uint8, device="cuda")
+    o = torch.empty((200, 24, 256), dtype=torch.float16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stv.stv_prefill_attn(shape, layer, stv.Seq(bad, 300), q, 200, "exact", ws, o, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & stv.STV_DEV_BAD_PAGE
+    # the context is still usable
+    assert np.all(np.isfinite(gpu_prefill(shape, layer, seq, q, 200, "exact")))
 
 
 def test_prefill_deterministic_and_rejects_bad_args(gpu):
