@@ -86,16 +86,17 @@ struct Ctl {
 };
 static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 
-// Waits poll first: this kernel's hand-offs (one per QK round) sit on the
-// critical path of every tile.
+// Waits suspend (try_wait with a time hint).  Polling waits measured 13 %
+// slower at 262K: with a dozen warps polling, the rounds' MMA-to-softmax
+// hand-offs (one per group) took longer to complete.
 __device__ __forceinline__ bool wait1(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
-  return stv::wait1<true>(b, parity, abort_flag);
+  return stv::wait1<false>(b, parity, abort_flag);
 }
 __device__ __forceinline__ bool waitw(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
-  return stv::waitw<true>(b, parity, abort_flag);
+  return stv::waitw<false>(b, parity, abort_flag);
 }
 __device__ __forceinline__ bool settle(uint64_t* b, uint32_t parity, uint32_t probed, volatile int* abort_flag) {
-  return stv::settle<true>(b, parity, probed, abort_flag);
+  return stv::settle<false>(b, parity, probed, abort_flag);
 }
 
 // Named barrier 1 over the four softmax warps, counting the threads whose
