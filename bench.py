@@ -379,8 +379,11 @@ def measure_prefill(dev, n: int = 32768, reps: int = 3, hq: int = 24, hkv: int =
     flops = 4.0 * hq * 256 * (n * (n + 1) / 2)
     peak, kind = measured_bf16_peak()
     tflops = flops / (ms * 1e-3) / 1e12
-    return {"prompt_tokens": n, "layers": 1, "path": path, "ms_per_call": ms, "tokens_per_s": n / (ms * 1e-3),
-            "bound": "tensor", "tflops": tflops, "peak_tflops": peak, "frac": tflops / peak, "peak_source": kind}
+    kernel = ("prefill_tc (persistent, one launch)" if path == "exact"
+              else "verify_i8 over 64-chunk launches + split_combine")
+    return {"prompt_tokens": n, "layers": 1, "path": path, "kernel": kernel, "ms_per_call": ms,
+            "tokens_per_s": n / (ms * 1e-3), "bound": "tensor", "tflops": tflops, "peak_tflops": peak,
+            "frac": tflops / peak, "peak_source": kind}
 
 
 def measure_format(w: workloads.Workload, p_accept: float, dev, kind: str, path: str = "exact", reps: int = 10):
@@ -584,6 +587,7 @@ def run_gpu(args, rank, world):
         r.set_trees(p_accept)
     lookup = measure_lookup(w, dev) if extra else None
     prefill = measure_prefill(dev) if extra else None
+    prefill_i8 = measure_prefill(dev, reps=1, path="int8") if extra else None
     int4 = measure_format(w, p_accept, dev, "int4", args.path) if extra and args.kv_format == "bit3" else None
     k4v2 = measure_format(w, p_accept, dev, "k4v2") if extra and args.kv_format == "bit3" else None
     if configs:
@@ -614,7 +618,7 @@ def run_gpu(args, rank, world):
                 vflops=vflops, peak=peak, peak_kind=peak_kind, achieved=achieved, clocks=clocks, status=st,
                 h2d=h2d, d2h=d2h, launches=launches_per_step(args, w) * args.steps, p_accept=p_accept,
                 traffic=traffic, round_gbs=bytes_lr / (us_per_lr * 1e-6) / 1e9 / world, lookup=lookup,
-                prefill=prefill, int4=int4, k4v2=k4v2, configs=configs)
+                prefill=prefill, prefill_i8=prefill_i8, int4=int4, k4v2=k4v2, configs=configs)
 
 
 KERNEL_SOURCES = {  # the files a verify launch's code comes from, per path and cache format
@@ -814,6 +818,7 @@ def main():
         "dev_status": res["status"],
         "configs": res["configs"],
         "next_rows": {"lookup_draft": res.get("lookup"), "prefill_attn": res.get("prefill"),
+                      "prefill_attn_int8": res.get("prefill_i8"),
                       "int4_cache_verify": res.get("int4"), "k4v2_cache_verify": res.get("k4v2")},
     }
     print(json.dumps(line), flush=True)
