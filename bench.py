@@ -368,13 +368,14 @@ def measure_prefill(dev, n: int = 32768, reps: int = 3, hq: int = 24, hkv: int =
     o = torch.empty((n, hq, 256), dtype=torch.float16, device=dev)
     stv.stv_prefill_attn(shape, layer, seq, q, n, path, ws, o)  # warm-up
     times = []
-    for _ in range(reps):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        stv.stv_prefill_attn(shape, layer, seq, q, n, path, ws, o)
-        b.record()
-        torch.cuda.synchronize()
-        times.append(a.elapsed_time(b))
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            stv.stv_prefill_attn(shape, layer, seq, q, n, path, ws, o)
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
     ms = statistics.median(times)
     flops = 4.0 * hq * 256 * (n * (n + 1) / 2)
     peak, kind = measured_bf16_peak()
@@ -383,7 +384,7 @@ def measure_prefill(dev, n: int = 32768, reps: int = 3, hq: int = 24, hkv: int =
               else "verify_i8 over 64-chunk launches + split_combine")
     return {"prompt_tokens": n, "layers": 1, "path": path, "kernel": kernel, "ms_per_call": ms,
             "tokens_per_s": n / (ms * 1e-3), "bound": "tensor", "tflops": tflops, "peak_tflops": peak,
-            "frac": tflops / peak, "peak_source": kind}
+            "frac": tflops / peak, "peak_source": kind, "clocks": clk.summary()}
 
 
 def measure_format(w: workloads.Workload, p_accept: float, dev, kind: str, path: str = "exact", reps: int = 10):
@@ -757,6 +758,9 @@ def main():
     ap.add_argument("--kv-format", default="bit3", choices=sorted(KV_FORMATS),
                     help="cache format: the 3-bit cache (default), the int4 per-token-head cache or the "
                          "K 4 / V 2-bit cache")
+    ap.add_argument("--prefill-only", type=int, default=None, metavar="N",
+                    help="time only prefill attention of an N-token prompt (on --path, --steps calls) and print its JSON "
+                         "(profiling captures of the prefill kernel)")
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip the other configs, lookup, prefill and other-format measurements "
                          "(profiling captures)")
@@ -772,6 +776,11 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             run_reference(args)
+        return
+    if args.prefill_only:
+        if rank == 0:
+            print(json.dumps({"prefill_attn": measure_prefill("cuda", n=args.prefill_only, reps=args.steps,
+                                                              path=args.path)}), flush=True)
         return
     if world > 1:
         import torch
