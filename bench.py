@@ -458,8 +458,11 @@ def graph_event():
 
 def time_round(r: GpuRound, path: str, steps: int, warmup: int, barrier, dev):
     """The round (L x append/verify/combine, accept, commit) captured once in
-    a CUDA graph, with event record nodes around each layer's verify launch;
-    `steps` replays timed with CUDA events, clocks sampled meanwhile.
+    a CUDA graph; `steps` replays timed with CUDA events, clocks sampled
+    meanwhile.  The verify launch times come from a second capture of the
+    same round with event record nodes around each layer's verify launch
+    (kept out of the timed graph: an event node between two launches
+    replaces their programmatic dependency with a full one).
     Returns the replay times (ms), the verify launch times (ms) and the clock
     summary."""
     import torch
@@ -476,7 +479,12 @@ def time_round(r: GpuRound, path: str, steps: int, warmup: int, barrier, dev):
         ev = None
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        r.step(path, verify_events=ev)
+        r.step(path)
+    graph_ev = None
+    if ev is not None:
+        graph_ev = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_ev):
+            r.step(path, verify_events=ev)
     for _ in range(warmup):
         graph.replay()
     marks = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
@@ -488,11 +496,14 @@ def time_round(r: GpuRound, path: str, steps: int, warmup: int, barrier, dev):
             marks[k + 1].record()
         barrier()
     round_ms = [marks[k].elapsed_time(marks[k + 1]) for k in range(steps)]
-    # per-launch verify time: the event nodes of a few more replays
+    # per-launch verify time: the event nodes of a few replays of the second graph
     verify_ms = []
+    if graph_ev is not None:
+        graph_ev.replay()  # its first replay uploads the graph
+        torch.cuda.synchronize()
     for _ in range(5):
-        if ev is not None:
-            graph.replay()
+        if graph_ev is not None:
+            graph_ev.replay()
             torch.cuda.synchronize()
             verify_ms += [a.elapsed_time(b) for a, b in ev]
         else:  # no event nodes: the same launches, eagerly, with events around verify
@@ -500,7 +511,7 @@ def time_round(r: GpuRound, path: str, steps: int, warmup: int, barrier, dev):
             r.step(path, verify_events=ev_eager)
             torch.cuda.synchronize()
             verify_ms += [a.elapsed_time(b) for a, b in ev_eager]
-    del graph
+    del graph, graph_ev
     return round_ms, verify_ms, clk.summary()
 
 

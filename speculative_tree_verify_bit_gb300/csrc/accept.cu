@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(32) tree_accept_kernel(const int32_t* __restri
                                                          const int32_t* __restrict__ argmax, int T,
                                                          int32_t* __restrict__ n_commit, int32_t* __restrict__ path,
                                                          int32_t* __restrict__ out_ids, int32_t* status) {
+  grid_dep_wait();
+  grid_dep_launch();
   const unsigned full = 0xffffffffu;
   const int s = blockIdx.x, i = threadIdx.x;
   const bool act = i < T;
@@ -92,8 +94,7 @@ __global__ void __launch_bounds__(32) tree_accept_kernel(const int32_t* __restri
 
 cudaError_t launch_tree_accept(const int32_t* parent, const int32_t* draft, const int32_t* argmax, int T, int n_seqs,
                                int32_t* n_commit, int32_t* path, int32_t* out_ids, int32_t* status, cudaStream_t s) {
-  tree_accept_kernel<<<n_seqs, 32, 0, s>>>(parent, draft, argmax, T, n_commit, path, out_ids, status);
-  return cudaGetLastError();
+  return launch_pdl(tree_accept_kernel, n_seqs, 32, 0, s, parent, draft, argmax, T, n_commit, path, out_ids, status);
 }
 
 }  // namespace stv

@@ -18,6 +18,8 @@
 namespace stv {
 
 __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ AppendParams p) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int row = blockIdx.x / p.hkv, h = blockIdx.x % p.hkv;
   const int c = threadIdx.x;
   const int s = __ldg(p.row_seq + row), pos = __ldg(p.row_pos + row);
@@ -43,6 +45,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ 
 // holds one channel's codes for 8 tokens, read-modify-written with atomics
 // (rows appended in the same launch may share it; their nibbles differ).
 __global__ void __launch_bounds__(256) kv_append_i4_kernel(const __grid_constant__ AppendParams p) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int row = blockIdx.x / p.hkv, h = blockIdx.x % p.hkv;
   const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
   __shared__ float red[2][kHeadDim / 32];
@@ -98,6 +102,8 @@ __global__ void __launch_bounds__(256) kv_append_i4_kernel(const __grid_constant
 // in the same launch may share it (their bits differ), so it is updated
 // with atomics.
 __global__ void __launch_bounds__(256) kv_append_k4v2_kernel(const __grid_constant__ AppendParams p) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int row = blockIdx.x / p.hkv, h = blockIdx.x % p.hkv;
   const int c = threadIdx.x, lane = c & 31, g = c >> 5;
   const int s = __ldg(p.row_seq + row), pos = __ldg(p.row_pos + row);
@@ -137,13 +143,10 @@ __global__ void __launch_bounds__(256) kv_append_k4v2_kernel(const __grid_consta
 
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t s) {
   if (p.n_rows == 0) return cudaSuccess;
-  if (p.fmt == kFmtInt4)
-    kv_append_i4_kernel<<<p.n_rows * p.hkv, 256, 0, s>>>(p);
-  else if (p.fmt == kFmtK4V2)
-    kv_append_k4v2_kernel<<<p.n_rows * p.hkv, 256, 0, s>>>(p);
-  else
-    kv_append_kernel<<<p.n_rows * p.hkv, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  const int blocks = p.n_rows * p.hkv;
+  if (p.fmt == kFmtInt4) return launch_pdl(kv_append_i4_kernel, blocks, 256, 0, s, p);
+  if (p.fmt == kFmtK4V2) return launch_pdl(kv_append_k4v2_kernel, blocks, 256, 0, s, p);
+  return launch_pdl(kv_append_kernel, blocks, 256, 0, s, p);
 }
 
 // ---------------------------------------------------------------------------
@@ -167,6 +170,8 @@ __device__ __forceinline__ bool commit_pages_ok(const SeqDesc& sd, const int* pa
 }
 
 __global__ void __launch_bounds__(256) kv_commit_kernel(const __grid_constant__ CommitParams p) {
+  grid_dep_wait();
+  grid_dep_launch();
   int b = blockIdx.x;
   const int h = b % p.hkv;
   b /= p.hkv;
@@ -260,6 +265,8 @@ __global__ void __launch_bounds__(256) kv_commit_kernel(const __grid_constant__ 
 // (validate the path, read every source row, then write), moving each row's
 // K codes and both scales whole and its V code channel by channel.
 __global__ void __launch_bounds__(256) kv_commit_i4_kernel(const __grid_constant__ CommitParams p) {
+  grid_dep_wait();
+  grid_dep_launch();
   int b = blockIdx.x;
   const int h = b % p.hkv;
   b /= p.hkv;
@@ -336,6 +343,8 @@ __global__ void __launch_bounds__(256) kv_commit_i4_kernel(const __grid_constant
 // path and every page, read every source row, then write), moving each row's
 // K codes and both scale rows whole and its V code channel by channel.
 __global__ void __launch_bounds__(256) kv_commit_k4v2_kernel(const __grid_constant__ CommitParams p) {
+  grid_dep_wait();
+  grid_dep_launch();
   int b = blockIdx.x;
   const int h = b % p.hkv;
   b /= p.hkv;
@@ -415,13 +424,9 @@ __global__ void __launch_bounds__(256) kv_commit_k4v2_kernel(const __grid_consta
 
 cudaError_t launch_kv_commit(const CommitParams& p, cudaStream_t s) {
   const int blocks = p.n_seqs * p.n_layers * p.hkv;
-  if (p.fmt == kFmtInt4)
-    kv_commit_i4_kernel<<<blocks, 256, 0, s>>>(p);
-  else if (p.fmt == kFmtK4V2)
-    kv_commit_k4v2_kernel<<<blocks, 256, 0, s>>>(p);
-  else
-    kv_commit_kernel<<<blocks, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  if (p.fmt == kFmtInt4) return launch_pdl(kv_commit_i4_kernel, blocks, 256, 0, s, p);
+  if (p.fmt == kFmtK4V2) return launch_pdl(kv_commit_k4v2_kernel, blocks, 256, 0, s, p);
+  return launch_pdl(kv_commit_kernel, blocks, 256, 0, s, p);
 }
 
 }  // namespace stv

@@ -138,6 +138,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   tc_before();
   __syncthreads();
   tc_after();
+  // Nothing above touches global memory: the previous kernel may still be running.
+  grid_dep_wait();
+  grid_dep_launch();
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == 0) {
@@ -511,8 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 cudaError_t launch_prefill(const PrefillParams& p, int grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  prefill_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(prefill_tc_kernel, grid, kThreads, kSmemBytes, s, p);
 }
 
 }  // namespace stv

@@ -9,6 +9,16 @@
 
 namespace stv {
 
+// Programmatic dependent launch: the round's kernels are launched with
+// programmatic stream serialization (launch_pdl), so a kernel's CTAs may be
+// scheduled while the previous kernel in the stream is still finishing.
+// grid_dep_wait() returns once that kernel has completed and its writes are
+// visible (at once when there is none); every kernel calls it before its
+// first global-memory access.  grid_dep_launch() lets the next kernel's CTAs
+// be scheduled; they wait in their own grid_dep_wait().
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void report(int32_t* status, int bit) {
   if (status) atomicOr(status, bit);
 }

@@ -180,6 +180,27 @@ struct CommitParams {
   int32_t* status;
 };
 
+// Launch with programmatic stream serialization (see grid_dep_wait in
+// stv_device.cuh): the kernel's CTAs may start while the previous kernel in
+// the stream finishes; every kernel of this library waits for it before its
+// first global-memory access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e != cudaSuccess) (void)cudaGetLastError();
+  return e;
+}
+
 // ---- host helpers (api.cu) ----
 int make_plan(const ShapeInfo& sh, const stv_seq* seqs, int n_seqs, int sm_count, Plan* plan);
 WsLayout ws_layout(const ShapeInfo& sh, int n_seqs, const Plan& plan);

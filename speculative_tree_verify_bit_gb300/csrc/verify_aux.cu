@@ -39,14 +39,15 @@ __device__ __forceinline__ void quantize_q_row_warp(const __half* __restrict__ q
 
 __global__ void __launch_bounds__(256) quantize_q_kernel(const __half* __restrict__ q, int n_rows,
                                                          int8_t* __restrict__ qi, float* __restrict__ sq) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= n_rows) return;
   quantize_q_row_warp(q + (int64_t)row * kHeadDim, qi + (int64_t)row * kHeadDim, sq + row);
 }
 
 cudaError_t launch_quantize_q(const __half* q, int n_rows, int8_t* qi, float* sq, cudaStream_t s) {
-  quantize_q_kernel<<<(n_rows + 7) / 8, 256, 0, s>>>(q, n_rows, qi, sq);
-  return cudaGetLastError();
+  return launch_pdl(quantize_q_kernel, (n_rows + 7) / 8, 256, 0, s, q, n_rows, qi, sq);
 }
 
 // ---------------------------------------------------------------------------
@@ -59,6 +60,8 @@ cudaError_t launch_quantize_q(const __half* q, int n_rows, int8_t* qi, float* sq
 // depend on timing.
 
 __global__ void __launch_bounds__(256) split_combine_kernel(const __grid_constant__ CombineParams p) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int quarter = gw & 3, row_id = gw >> 2;
   int s = 0, base = 0;
@@ -114,8 +117,7 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const __grid_constan
 
 cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t s) {
   const int warps = p.n_seqs * p.hkv * p.R * 4;  // four channel quarters per row
-  split_combine_kernel<<<(warps + 7) / 8, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(split_combine_kernel, (warps + 7) / 8, 256, 0, s, p);
 }
 
 // ---------------------------------------------------------------------------
@@ -123,14 +125,15 @@ cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t s) {
 // prompt tokens, whose ancestor-or-self masks are the causal mask.
 
 __global__ void __launch_bounds__(256) chain_parents_t_kernel(int32_t* parent, int chunks, int t) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int i = blockIdx.x * 256 + threadIdx.x;
   if (i < chunks * t) parent[i] = (i % t) - 1;
 }
 
 cudaError_t launch_chain_parents(int32_t* parent, int chunks, int t, cudaStream_t s) {
   const int n = chunks * t;
-  chain_parents_t_kernel<<<(n + 255) / 256, 256, 0, s>>>(parent, chunks, t);
-  return cudaGetLastError();
+  return launch_pdl(chain_parents_t_kernel, (n + 255) / 256, 256, 0, s, parent, chunks, t);
 }
 
 }  // namespace stv

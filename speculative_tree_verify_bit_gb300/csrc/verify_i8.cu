@@ -178,6 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_con
     ctl->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  // Nothing above touches global memory: the previous kernel may still be running.
+  grid_dep_wait();
   if (tid < T) {  // a2: ancestor-or-self masks
     uint32_t m = 1u << tid;
     int n = tid;
@@ -203,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_con
   tc_before();
   __syncthreads();
   tc_after();
+  grid_dep_launch();
   const uint32_t tmem = ctl->tmem_base;
 
   if (warp == 0) {
@@ -720,8 +723,7 @@ cudaError_t launch_one(const VerifyParams& p, cudaStream_t s) {
   auto kernel = verify_i8_kernel<kAppend, kWithhold>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  kernel<<<p.n_units, kThreads, kSmemBytes, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kernel, p.n_units, kThreads, kSmemBytes, s, p);
 }
 
 }  // namespace

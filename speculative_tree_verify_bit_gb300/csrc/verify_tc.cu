@@ -180,6 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
     bars->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  // Nothing above touches global memory: the previous kernel may still be running.
+  grid_dep_wait();
   if (tid < T) {  // a2: ancestor-or-self masks
     uint32_t m = 1u << tid;
     int n = tid;
@@ -205,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
   tc_before();
   __syncthreads();
   tc_after();
+  grid_dep_launch();
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == 0) {
@@ -740,8 +743,7 @@ cudaError_t launch_one(const VerifyParams& p, cudaStream_t s) {
   constexpr int smem = Fmt<kFmt>::smem;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kernel<<<p.n_units, kThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kernel, p.n_units, kThreads, smem, s, p);
 }
 
 }  // namespace
