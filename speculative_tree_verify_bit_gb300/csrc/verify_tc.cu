@@ -107,7 +107,6 @@ struct Bars {
   uint64_t tree_packed;  // the round's tree rows of this unit are in the cache (fused append)
   uint32_t tmem_base;
   int abort;
-  uint32_t anc[kMaxT];
 };
 
 static_assert(sizeof(Bars) <= 1024, "barrier block");
@@ -182,21 +181,18 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
   }
   // Nothing above touches global memory: the previous kernel may still be running.
   grid_dep_wait();
-  if (tid < T) {  // a2: ancestor-or-self masks
-    uint32_t m = 1u << tid;
-    int n = tid;
-    const int32_t* par = p.parent + (int64_t)s * T;
-    for (int st = 0; st < T && n > 0; ++st) {
-      int pa = __ldg(par + n);
-      if (pa < 0 || pa >= n) {
-        if (split == 0 && h == 0) report(p.status, STV_DEV_BAD_TREE);
-        break;
-      }
-      m |= 1u << pa;
-      n = pa;
+  // Start the first global reads' trips to L2 before the set-up barrier:
+  // the producer's first page-table line and the softmax threads' Q rows.
+  if (tid == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(sd.page_table + (tok0 >> 8)));
+  if (warp >= 2 && warp < 6) {
+    const int r = (warp & 3) * 32 + lane;
+    if (r < R) {
+      const char* qr = p.path == STV_PATH_INT8
+                           ? reinterpret_cast<const char*>(p.qi + (((int64_t)s * T + r / G) * p.hq + h * G + r % G) * kHeadDim)
+                           : reinterpret_cast<const char*>(p.q + (((int64_t)s * T + r / G) * p.hq + h * G + r % G) * kHeadDim);
+      const int lines = p.path == STV_PATH_INT8 ? 2 : 4;  // 256 int8 or 512 fp16 bytes
+      for (int ln = 0; ln < lines; ++ln) asm volatile("prefetch.global.L2 [%0];" ::"l"(qr + 128 * ln));
     }
-    if (tid == 0 && __ldg(par) != -1 && split == 0 && h == 0) report(p.status, STV_DEV_BAD_TREE);
-    bars->anc[tid] = m;
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&bars->tmem_base)),
@@ -341,7 +337,23 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->q_ready);
     }
-    const uint32_t anc = bars->anc[node];
+    // a2: this row's ancestor-or-self mask, from parent[] (only the tiles
+    // that hold tree keys use it, so its loads overlap the first tiles)
+    uint32_t anc = 1u << node;
+    {
+      int n = node;
+      const int32_t* par = p.parent + (int64_t)s * T;
+      for (int st = 0; st < T && n > 0; ++st) {
+        const int pa = __ldg(par + n);
+        if (pa < 0 || pa >= n) {
+          if (split == 0 && h == 0) report(p.status, STV_DEV_BAD_TREE);
+          break;
+        }
+        anc |= 1u << pa;
+        n = pa;
+      }
+      if (r == 0 && __ldg(par) != -1 && split == 0 && h == 0) report(p.status, STV_DEV_BAD_TREE);
+    }
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
