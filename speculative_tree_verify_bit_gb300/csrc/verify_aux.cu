@@ -52,12 +52,23 @@ cudaError_t launch_quantize_q(const __half* q, int n_rows, int8_t* qi, float* sq
 
 // ---------------------------------------------------------------------------
 // a5: split_combine.  One warp per (sequence, KV head, row, 64-channel
-// quarter); lane = 2 channels.  The warp reads a chunk of up to 32 splits'
-// (m, l) at once (split kb + j in lane j), forms M = max m and the weights
-// 2^(m - M), then issues the chunk's partial-O loads together (a fully
-// unrolled, predicated loop: one memory round trip per chunk rather than
-// one per split) and sums them in split order, so the result does not
+// quarter); lane = 2 channels.  Split kb + j's (m, l) sits in lane j of
+// chunk kb / 32.  The (m, l) of every split and the partial O of the first
+// two chunks of 32 splits are loaded together, one memory round trip for up
+// to 64 splits (later chunks take one more each); then M = max m, the
+// weights 2^(m - M), and the sums in split order, so the result does not
 // depend on timing.
+
+// acc += the chunk's 32 partials weighted by w (lane j's weight is split j's)
+__device__ __forceinline__ void combine_chunk(const float2 (&o)[32], float w, float& acc0, float& acc1) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float wk = __shfl_sync(0xffffffffu, w, j);
+    // a split with weight 0 (no visible key for this row) adds nothing
+    acc0 = wk != 0.f ? fmaf(wk, o[j].x, acc0) : acc0;
+    acc1 = wk != 0.f ? fmaf(wk, o[j].y, acc1) : acc1;
+  }
+}
 
 __global__ void __launch_bounds__(256) split_combine_kernel(const __grid_constant__ CombineParams p) {
   grid_dep_wait();
@@ -74,38 +85,48 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const __grid_constan
   const SeqDesc& sd = p.seq[s];
   const int u0 = sd.unit_base + h * sd.splits, splits = sd.splits;
   const float2* ml = reinterpret_cast<const float2*>(p.ml);
+  const int64_t split_stride = (int64_t)p.R * kHeadDim;
+  const float* src = p.o_part + (int64_t)u0 * split_stride + (int64_t)r * kHeadDim + quarter * 64 + lane * 2;
   // (m, l) of every split, 32 per register: at most kMaxChunks * 32 splits
   constexpr int kMaxChunks = kMaxSplitsPerHead / 32;
   float2 mlv[kMaxChunks];
-  float M = -INFINITY;
 #pragma unroll
   for (int c = 0; c < kMaxChunks; ++c) {
     const int k = c * 32 + lane;
     mlv[c] = k < splits ? ml[(int64_t)(u0 + k) * p.R + r] : make_float2(-INFINITY, 0.f);
-    M = fmaxf(M, mlv[c].x);
   }
+  // the partials of chunks 0 and 1, in flight with the (m, l) loads
+  float2 oa[32], ob[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    oa[j] = j < splits ? *reinterpret_cast<const float2*>(src + j * split_stride) : make_float2(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    ob[j] = 32 + j < splits ? *reinterpret_cast<const float2*>(src + (32 + j) * split_stride) : make_float2(0.f, 0.f);
+  float M = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < kMaxChunks; ++c) M = fmaxf(M, mlv[c].x);
   M = wmax(M);
   float L = 0.f, acc0 = 0.f, acc1 = 0.f;
-  const int64_t split_stride = (int64_t)p.R * kHeadDim;
-  const float* src = p.o_part + (int64_t)u0 * split_stride + (int64_t)r * kHeadDim + quarter * 64 + lane * 2;
+  auto weight = [&](const float2 v) {
+    const float w = v.x == -INFINITY ? 0.f : exp2f(v.x - M);
+    L += w * v.y;
+    return w;
+  };
+  combine_chunk(oa, weight(mlv[0]), acc0, acc1);
+  if (splits > 32) combine_chunk(ob, weight(mlv[1]), acc0, acc1);
+  // chunks 2 and later (more than 64 splits: contexts past about 500K keys)
 #pragma unroll 1
-  for (int c = 0; c < kMaxChunks && c * 32 < splits; ++c) {
-    const float w = mlv[0].x == -INFINITY ? 0.f : exp2f(mlv[0].x - M);
-    L += w * mlv[0].y;
+  for (int c = 2; c < kMaxChunks && c * 32 < splits; ++c) {
+    float w = 0.f;
 #pragma unroll
-    for (int i = 0; i + 1 < kMaxChunks; ++i) mlv[i] = mlv[i + 1];  // next chunk to [0], in registers
+    for (int i = 2; i < kMaxChunks; ++i)
+      if (i == c) w = weight(mlv[i]);
     const int n = min(32, splits - c * 32);
     const float* sp = src + (int64_t)(c * 32) * split_stride;
-    float2 o[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) o[j] = j < n ? *reinterpret_cast<const float2*>(sp + j * split_stride) : make_float2(0.f, 0.f);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float wk = __shfl_sync(0xffffffffu, w, j);
-      // a split with weight 0 (no visible key for this row) adds nothing
-      acc0 = wk != 0.f ? fmaf(wk, o[j].x, acc0) : acc0;
-      acc1 = wk != 0.f ? fmaf(wk, o[j].y, acc1) : acc1;
-    }
+    for (int j = 0; j < 32; ++j) oa[j] = j < n ? *reinterpret_cast<const float2*>(sp + j * split_stride) : make_float2(0.f, 0.f);
+    combine_chunk(oa, w, acc0, acc1);
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
