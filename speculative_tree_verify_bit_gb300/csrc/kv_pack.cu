@@ -22,6 +22,10 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ 
   grid_dep_launch();
   const int row = blockIdx.x / p.hkv, h = blockIdx.x % p.hkv;
   const int c = threadIdx.x;
+  // The row's values first: they depend on nothing else, so their memory
+  // round trip overlaps the row's sequence/position and page-table reads.
+  const int64_t src = ((int64_t)row * p.hkv + h) * kHeadDim + c;
+  const float xk = __half2float(p.k[src]), xv = __half2float(p.v[src]);
   const int s = __ldg(p.row_seq + row), pos = __ldg(p.row_pos + row);
   if (s < 0 || s >= p.n_seqs || pos < 0) {
     if (c == 0) report(p.status, STV_DEV_BAD_ROW);
@@ -31,9 +35,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ 
       head_block(p.seq[s], p.pool, p.page_bytes, p.pool_pages, pos, h, c == 0 ? p.status : nullptr));
   if (!hb) return;
   const int slot = pos & (kPageTok - 1);
-  const int64_t src = ((int64_t)row * p.hkv + h) * kHeadDim + c;
-
-  append_row_channel(__half2float(p.k[src]), __half2float(p.v[src]), hb, slot, c);
+  append_row_channel(xk, xv, hb, slot, c);
 }
 
 // The int4 per-token-head cache (include/stv.h, group 256): one CTA per
@@ -50,6 +52,9 @@ __global__ void __launch_bounds__(256) kv_append_i4_kernel(const __grid_constant
   const int row = blockIdx.x / p.hkv, h = blockIdx.x % p.hkv;
   const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
   __shared__ float red[2][kHeadDim / 32];
+  // the row's values first (see kv_append_kernel)
+  const int64_t src = ((int64_t)row * p.hkv + h) * kHeadDim + c;
+  const float xk = __half2float(p.k[src]), xv = __half2float(p.v[src]);
   const int s = __ldg(p.row_seq + row), pos = __ldg(p.row_pos + row);
   if (s < 0 || s >= p.n_seqs || pos < 0) {
     if (c == 0) report(p.status, STV_DEV_BAD_ROW);
@@ -59,8 +64,6 @@ __global__ void __launch_bounds__(256) kv_append_i4_kernel(const __grid_constant
                                                 c == 0 ? p.status : nullptr, kI4HeadBytes));
   if (!hb) return;
   const int slot = pos & (kPageTok - 1);
-  const int64_t src = ((int64_t)row * p.hkv + h) * kHeadDim + c;
-  const float xk = __half2float(p.k[src]), xv = __half2float(p.v[src]);
   const float mk = warp_max(fabsf(xk)), mv = warp_max(fabsf(xv));
   if (lane == 0) {
     red[0][warp] = mk;
@@ -106,6 +109,9 @@ __global__ void __launch_bounds__(256) kv_append_k4v2_kernel(const __grid_consta
   grid_dep_launch();
   const int row = blockIdx.x / p.hkv, h = blockIdx.x % p.hkv;
   const int c = threadIdx.x, lane = c & 31, g = c >> 5;
+  // the row's values first (see kv_append_kernel)
+  const int64_t src = ((int64_t)row * p.hkv + h) * kHeadDim + c;
+  const float xk = __half2float(p.k[src]), xv = __half2float(p.v[src]);
   const int s = __ldg(p.row_seq + row), pos = __ldg(p.row_pos + row);
   if (s < 0 || s >= p.n_seqs || pos < 0) {
     if (c == 0) report(p.status, STV_DEV_BAD_ROW);
@@ -115,8 +121,6 @@ __global__ void __launch_bounds__(256) kv_append_k4v2_kernel(const __grid_consta
       head_block(p.seq[s], p.pool, p.page_bytes, p.pool_pages, pos, h, c == 0 ? p.status : nullptr, kKv2HeadBytes));
   if (!hb) return;
   const int slot = pos & (kPageTok - 1);
-  const int64_t src = ((int64_t)row * p.hkv + h) * kHeadDim + c;
-  const float xk = __half2float(p.k[src]), xv = __half2float(p.v[src]);
   // K, 4 bits
   const __half sk = __float2half_rn(warp_max(fabsf(xk)) * 0.125f);
   const float skf = __half2float(sk);
