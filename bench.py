@@ -387,6 +387,62 @@ def measure_prefill(dev, n: int = 32768, reps: int = 3, hq: int = 24, hkv: int =
             "frac": tflops / peak, "peak_source": kind, "clocks": clk.summary()}
 
 
+def measure_ctx_sweep(dev, ctxs=(0, 1024, 4096, 8192, 16384, 32768, 65536, 131072, 262144), reps: int = 15,
+                      hq: int = 24, hkv: int = 4, t: int = 16):
+    """verify_attn and split_combine launch times against context length: one
+    sequence, one layer, T = 16 (a chain tree), exact path; L2 flushed before
+    each timed pair, each launch on its own (so each pays its whole fixed
+    part: launch, set-up, pipeline fill, epilogue).  A least-squares line
+    through the points from 16K keys up, where the split plan gives about one
+    work unit per SM, separates the fixed part from the cost per key."""
+    import torch
+
+    import speculative_tree_verify_bit_gb300 as stv
+
+    shape = stv.make_shape(hq, hkv)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    points = []
+    for ctx in ctxs:
+        pages = workloads.pages_needed(ctx, t) + 1
+        table = torch.as_tensor(np.random.default_rng(5).permutation(pages).astype(np.int32), device=dev)
+        layer = stv.LayerCache.empty(pages, hkv, device=dev)
+        k, v = workloads.kv_rows(77, ctx + t, hkv, device=dev)
+        stv.stv_kv_append_pack(shape, layer, [stv.Seq(table, 0)], k.contiguous(), v.contiguous(),
+                               torch.zeros(ctx + t, dtype=torch.int32, device=dev),
+                               torch.arange(ctx + t, dtype=torch.int32, device=dev))
+        seqs = [stv.Seq(table, ctx)]
+        q = workloads.q_rows(78, 1, t, hq, device=dev).contiguous()
+        parent = torch.as_tensor(workloads.chain_tree(t)[None], device=dev)
+        ws = torch.empty(stv.stv_verify_workspace_bytes(shape, seqs, t), dtype=torch.uint8, device=dev)
+        o = torch.empty((1, t, hq, 256), dtype=torch.float16, device=dev)
+        for _ in range(3):
+            stv.stv_verify_attn(shape, layer, seqs, q, parent, t, "exact", ws)
+            stv.stv_split_combine(shape, seqs, t, ws, o)
+        tv, tc = [], []
+        for _ in range(reps):
+            flush.fill_(1)
+            a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            a.record()
+            stv.stv_verify_attn(shape, layer, seqs, q, parent, t, "exact", ws)
+            b.record()
+            stv.stv_split_combine(shape, seqs, t, ws, o)
+            c.record()
+            torch.cuda.synchronize()
+            tv.append(a.elapsed_time(b) * 1e3)
+            tc.append(b.elapsed_time(c) * 1e3)
+        points.append({"ctx": ctx, "verify_us": statistics.median(tv), "combine_us": statistics.median(tc)})
+        del layer, ws
+        torch.cuda.empty_cache()
+    xs = [p["ctx"] for p in points if p["ctx"] >= 16384]
+    ys = [p["verify_us"] for p in points if p["ctx"] >= 16384]
+    fit = None
+    if len(xs) >= 2:
+        slope, icpt = np.polyfit(np.asarray(xs, float), np.asarray(ys, float), 1)
+        fit = {"fixed_us": float(icpt), "us_per_1k_keys": float(slope * 1024), "from_ctx": 16384}
+    return {"points": points, "fit": fit, "l2": "flushed before each timed launch pair", "path": "exact",
+            "t_nodes": t, "hq": hq, "hkv": hkv}
+
+
 def measure_format(w: workloads.Workload, p_accept: float, dev, kind: str, path: str = "exact", reps: int = 10):
     """The same round over another cache format (the int4 per-token-head
     cache, or the K 4 / V 2-bit cache): two layers resident, eager rounds with
@@ -772,6 +828,9 @@ def main():
     ap.add_argument("--prefill-only", type=int, default=None, metavar="N",
                     help="time only prefill attention of an N-token prompt (on --path, --steps calls) and print its JSON "
                          "(profiling captures of the prefill kernel)")
+    ap.add_argument("--ctx-sweep", action="store_true",
+                    help="time verify_attn and split_combine launches alone against context length, one "
+                         "layer, and print their JSON (the fixed part of a launch and the cost per key)")
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip the other configs, lookup, prefill and other-format measurements "
                          "(profiling captures)")
@@ -787,6 +846,10 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             run_reference(args)
+        return
+    if args.ctx_sweep:
+        if rank == 0:
+            print(json.dumps({"ctx_sweep": measure_ctx_sweep("cuda")}), flush=True)
         return
     if args.prefill_only:
         if rank == 0:
