@@ -247,6 +247,31 @@ class GpuRound:
         self.path = torch.zeros((n, T), dtype=torch.int32, device=device)
         self.out_ids = torch.zeros((n, T), dtype=torch.int32, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        # A round's inputs (Q, tree K/V rows, trees) and its results (commit
+        # counts, accepted ids) each live in one device buffer, as a serving
+        # engine stages them: one host-to-device copy per round in, one out.
+        self.inputs, views = self._stage(self.q + self.k_tree + self.v_tree + [self.parent, self.draft, self.argmax])
+        L = self.L
+        self.q, self.k_tree, self.v_tree = views[:L], views[L:2 * L], views[2 * L:3 * L]
+        self.parent, self.draft, self.argmax = views[3 * L:]
+        self.outputs, (self.n_commit, self.out_ids) = self._stage([self.n_commit, self.out_ids])
+
+    def _stage(self, tensors):
+        """One contiguous device buffer holding copies of `tensors`, each
+        256-byte aligned; returns it and the tensors' views into it."""
+        torch = self.torch
+        sizes = [t.numel() * t.element_size() for t in tensors]
+        offs, at = [], 0
+        for sz in sizes:
+            offs.append(at)
+            at += (sz + 255) // 256 * 256
+        buf = torch.zeros(at, dtype=torch.uint8, device=self.dev)
+        views = []
+        for t, off, sz in zip(tensors, offs, sizes):
+            v = buf[off:off + sz].view(t.dtype).view(t.shape)
+            v.copy_(t)
+            views.append(v)
+        return buf, views
 
     def set_trees(self, p_accept: float):
         """Draw the round's trees for another acceptance probability into the
@@ -285,17 +310,9 @@ class GpuRound:
 def e2e_step(r: GpuRound, host, path):
     """The same round through the public API with host buffers: copy the
     round's inputs in from pinned memory, run it, read the accepted tokens."""
-    torch = r.torch
-    for l in range(r.L):
-        r.q[l].copy_(host["q"][l], non_blocking=True)
-        r.k_tree[l].copy_(host["k"][l], non_blocking=True)
-        r.v_tree[l].copy_(host["v"][l], non_blocking=True)
-    r.parent.copy_(host["parent"], non_blocking=True)
-    r.draft.copy_(host["draft"], non_blocking=True)
-    r.argmax.copy_(host["argmax"], non_blocking=True)
+    r.inputs.copy_(host["inputs"], non_blocking=True)
     r.step(path)
-    host["n_commit"].copy_(r.n_commit, non_blocking=True)
-    host["out_ids"].copy_(r.out_ids, non_blocking=True)
+    host["outputs"].copy_(r.outputs, non_blocking=True)
 
 
 def measure_lookup(w: workloads.Workload, dev, reps: int = 50, min_len: int = 6, max_len: int = 12, k: int = 15):
@@ -611,17 +628,12 @@ def run_gpu(args, rank, world):
     round_ms, verify_ms, clocks = time_round(r, args.path, args.steps, args.warmup, barrier, dev)
     st = int(r.status.item())
 
-    # e2e: host buffers, copies inside the timed region
-    host = {
-        "q": [x.cpu().pin_memory() for x in r.q], "k": [x.cpu().pin_memory() for x in r.k_tree],
-        "v": [x.cpu().pin_memory() for x in r.v_tree], "parent": r.parent.cpu().pin_memory(),
-        "draft": r.draft.cpu().pin_memory(), "argmax": r.argmax.cpu().pin_memory(),
-        "n_commit": torch.zeros_like(r.n_commit, device="cpu").pin_memory(),
-        "out_ids": torch.zeros_like(r.out_ids, device="cpu").pin_memory(),
-    }
-    h2d = sum(x.numel() * x.element_size() for k in ("q", "k", "v") for x in host[k]) + sum(
-        host[k].numel() * 4 for k in ("parent", "draft", "argmax"))
-    d2h = host["n_commit"].numel() * 4 + host["out_ids"].numel() * 4
+    # e2e: the round's inputs copied in from pinned host memory (one buffer:
+    # Q and the tree K/V rows of every layer, the trees) and its results read
+    # back (commit counts, accepted ids), both inside the timed region
+    host = {"inputs": r.inputs.cpu().pin_memory(), "outputs": torch.zeros_like(r.outputs, device="cpu").pin_memory()}
+    h2d = host["inputs"].numel()
+    d2h = host["outputs"].numel()
     for _ in range(2):
         e2e_step(r, host, args.path)
     barrier()
