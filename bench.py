@@ -301,10 +301,15 @@ class GpuRound:
             if verify_events is not None:
                 verify_events[l][1].record()
             stv.stv_split_combine(self.shape, self.seqs, self.T, self.ws, self.o)
+        timed_tail = verify_events is not None and len(verify_events) > self.L
+        if timed_tail:  # one more event pair: around acceptance and commit
+            verify_events[self.L][0].record()
         stv.stv_tree_accept(self.parent, self.draft, self.argmax, self.n_commit, self.path, self.out_ids,
                             dev_status=self.status)
         stv.stv_kv_commit(self.shape, self.layers, self.seqs, self.T, self.n_commit, self.path,
                           dev_status=self.status)
+        if timed_tail:
+            verify_events[self.L][1].record()
 
 
 def e2e_step(r: GpuRound, host, path):
@@ -547,7 +552,7 @@ def time_round(r: GpuRound, path: str, steps: int, warmup: int, barrier, dev):
             r.step(path)
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    ev = [[graph_event(), graph_event()] for _ in range(r.L)]
+    ev = [[graph_event(), graph_event()] for _ in range(r.L + 1)]  # each verify, then accept + commit
     if any(e is None for pair in ev for e in pair):
         ev = None
     graph = torch.cuda.CUDAGraph()
@@ -571,6 +576,7 @@ def time_round(r: GpuRound, path: str, steps: int, warmup: int, barrier, dev):
     round_ms = [marks[k].elapsed_time(marks[k + 1]) for k in range(steps)]
     # per-launch verify time: the event nodes of a few replays of the second graph
     verify_ms = []
+    r.accept_commit_ms = []
     if graph_ev is not None:
         graph_ev.replay()  # its first replay uploads the graph
         torch.cuda.synchronize()
@@ -578,7 +584,8 @@ def time_round(r: GpuRound, path: str, steps: int, warmup: int, barrier, dev):
         if graph_ev is not None:
             graph_ev.replay()
             torch.cuda.synchronize()
-            verify_ms += [a.elapsed_time(b) for a, b in ev]
+            verify_ms += [a.elapsed_time(b) for a, b in ev[:r.L]]
+            r.accept_commit_ms.append(ev[r.L][0].elapsed_time(ev[r.L][1]))
         else:  # no event nodes: the same launches, eagerly, with events around verify
             ev_eager = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(r.L)]
             r.step(path, verify_events=ev_eager)
@@ -626,6 +633,7 @@ def run_gpu(args, rank, world):
         torch.cuda.synchronize()
 
     round_ms, verify_ms, clocks = time_round(r, args.path, args.steps, args.warmup, barrier, dev)
+    ac_us = statistics.median(r.accept_commit_ms) * 1e3 if r.accept_commit_ms else None
     st = int(r.status.item())
 
     # e2e: the round's inputs copied in from pinned host memory (one buffer:
@@ -698,7 +706,7 @@ def run_gpu(args, rank, world):
                 vflops=vflops, peak=peak, peak_kind=peak_kind, achieved=achieved, clocks=clocks, status=st,
                 h2d=h2d, d2h=d2h, launches=launches_per_step(args, w) * args.steps, p_accept=p_accept,
                 traffic=traffic, round_gbs=bytes_lr / (us_per_lr * 1e-6) / 1e9 / world, lookup=lookup,
-                prefill=prefill, prefill_i8=prefill_i8, int4=int4, k4v2=k4v2, configs=configs)
+                prefill=prefill, prefill_i8=prefill_i8, int4=int4, k4v2=k4v2, configs=configs, ac_us=ac_us)
 
 
 KERNEL_SOURCES = {  # the files a verify launch's code comes from, per path and cache format
@@ -895,6 +903,7 @@ def main():
         "gbs_per_layer_round": res["round_gbs"],
         "bytes_per_layer_round": res["bytes_lr"],
         "verify_us_per_launch": res["v_us"],
+        "accept_commit_us_per_round": res.get("ac_us"),
         # The verify launch's arithmetic intensity (FLOPs per algorithmic byte)
         # is above the GPU's ridge point, so its roofline is the dense fp16
         # tensor peak; the HBM figures are beside it.
