@@ -29,6 +29,12 @@
  *    never allocates, frees or synchronises, and keeps no pointer after the
  *    call returns.  All work is enqueued on `stream` (NULL = legacy default
  *    stream); asynchronous CUDA faults surface at the caller's next sync.
+ *  - Kernels are launched with programmatic stream serialization: a launch's
+ *    blocks may be scheduled, and do their set-up, while the previous kernel
+ *    in the stream is still running, but every kernel waits for that kernel
+ *    to complete (and its writes to be visible) before its first read or
+ *    write of global memory.  Stream order is kept for any predecessor, the
+ *    library's own or not.
  *  - Data that lives on the device (page tables, row positions, parent
  *    arrays, commit counts) cannot be checked on the host.  Kernels check it
  *    as they read it, never touch memory outside the described buffers, and
