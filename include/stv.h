@@ -363,6 +363,21 @@ int stv_prefill_attn(const stv_shape* shape, const stv_layer_cache* layer, const
                      stv_stream_t stream);
 
 /*
+ * Failure-path test of stv_prefill_attn's persistent kernel (exact path, the
+ * 3-bit cache; the pages have no counterpart: it exists to test this
+ * library's failure detection without a GPU fault).  Same arguments and
+ * checks as stv_prefill_attn; the kernel's producer issues none of its
+ * copies, so every wait on them gives up after its bound (about 1.3 s), the
+ * kernel stops every role, waits for anything it issued, frees its tensor
+ * memory, ORs STV_DEV_TIMEOUT into *dev_status and returns.  `o` is then
+ * invalid; the CUDA context stays usable.  STV_ERR_UNIMPLEMENTED for the
+ * int8 path and the other cache formats.
+ */
+int stv_prefill_attn_timeout_test(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seq,
+                                  const void* q, int n_tokens, int path, void* workspace, size_t ws_bytes, void* o,
+                                  int32_t* dev_status, stv_stream_t stream);
+
+/*
  * Lookup drafting (next row f4).  Reddit posts (u/iamMess), "Now added" list,
  * lookup-augmented drafting (draft tokens copied from earlier in the same
  * request: find where its trailing tokens, between six and twelve of them,

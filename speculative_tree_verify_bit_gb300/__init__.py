@@ -49,6 +49,7 @@ EXPORTS = (
     "stv_verify_attn", "stv_split_combine", "stv_tree_accept", "stv_kv_commit", "stv_int8_qk_dots",
     "stv_verify_attn_no_alloc", "stv_append_verify_attn", "stv_lookup_workspace_bytes", "stv_lookup_draft",
     "stv_prefill_workspace_bytes", "stv_prefill_attn", "stv_verify_attn_timeout_test",
+    "stv_prefill_attn_timeout_test",
 )
 
 
@@ -396,6 +397,21 @@ def stv_prefill_attn(shape, layer: LayerCache, seq, q, n_tokens: int, path, work
     arr = _seq_array([seq])
     path = PATHS.get(path, path)
     _check("stv_prefill_attn", load().stv_prefill_attn(
+        ctypes.byref(shape), ctypes.byref(lc), arr, _ptr(q, torch.float16, "q"), int(n_tokens), int(path),
+        _ptr(workspace, name="workspace"), workspace.numel() * workspace.element_size(),
+        _ptr(o, torch.float16, "o"), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+
+
+def stv_prefill_attn_timeout_test(shape, layer: LayerCache, seq, q, n_tokens: int, path, workspace, o,
+                                  dev_status=None, stream=None):
+    """stv_prefill_attn with the persistent kernel's copies withheld: every
+    wait runs out and the kernel reports STV_DEV_TIMEOUT (failure-path test)."""
+    import torch
+
+    lc = layer.c()
+    arr = _seq_array([seq])
+    path = PATHS.get(path, path)
+    _check("stv_prefill_attn_timeout_test", load().stv_prefill_attn_timeout_test(
         ctypes.byref(shape), ctypes.byref(lc), arr, _ptr(q, torch.float16, "q"), int(n_tokens), int(path),
         _ptr(workspace, name="workspace"), workspace.numel() * workspace.element_size(),
         _ptr(o, torch.float16, "o"), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))

@@ -363,9 +363,9 @@ int stv_prefill_workspace_bytes(const stv_shape* shape, const stv_seq* seq, int 
   return STV_OK;
 }
 
-int stv_prefill_attn(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seq, const void* q,
-                     int n_tokens, int path, void* workspace, size_t ws_bytes, void* o, int32_t* dev_status,
-                     stv_stream_t stream) {
+static int prefill_common(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seq, const void* q,
+                          int n_tokens, int path, void* workspace, size_t ws_bytes, void* o, int32_t* dev_status,
+                          stv_stream_t stream, bool withhold_copies) {
   size_t need = 0;
   int rc = stv_prefill_workspace_bytes(shape, seq, n_tokens, &need);
   if (rc) return rc;
@@ -398,8 +398,9 @@ int stv_prefill_attn(const stv_shape* shape, const stv_layer_cache* layer, const
     pp.status = dev_status;
     int sms = 0;
     if ((rc = device_sm_count(&sms))) return rc;
-    return to_status(launch_prefill(pp, std::min(pp.n_units, sms), (cudaStream_t)stream));
+    return to_status(launch_prefill(pp, std::min(pp.n_units, sms), (cudaStream_t)stream, withhold_copies));
   }
+  if (withhold_copies) return STV_ERR_UNIMPLEMENTED;  // the failure-path test runs the persistent kernel only
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int32_t* parents = reinterpret_cast<int32_t*>(ws);
   // chain parents for STV_MAX_SEQS chunks of c tokens; a last partial chunk
@@ -419,6 +420,18 @@ int stv_prefill_attn(const stv_shape* shape, const stv_layer_cache* layer, const
       return r;
     return stv_split_combine(shape, seqs, pl.count, pl.t, ws + kParentsBytes, ws_bytes - kParentsBytes, os, stream);
   });
+}
+
+int stv_prefill_attn(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seq, const void* q,
+                     int n_tokens, int path, void* workspace, size_t ws_bytes, void* o, int32_t* dev_status,
+                     stv_stream_t stream) {
+  return prefill_common(shape, layer, seq, q, n_tokens, path, workspace, ws_bytes, o, dev_status, stream, false);
+}
+
+int stv_prefill_attn_timeout_test(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seq,
+                                  const void* q, int n_tokens, int path, void* workspace, size_t ws_bytes, void* o,
+                                  int32_t* dev_status, stv_stream_t stream) {
+  return prefill_common(shape, layer, seq, q, n_tokens, path, workspace, ws_bytes, o, dev_status, stream, true);
 }
 
 int stv_tree_accept(const int32_t* parent, const int32_t* draft_ids, const int32_t* target_argmax, int t_nodes,

@@ -92,6 +92,9 @@ __device__ __forceinline__ Unit unit_info(const PrefillParams& p, int u) {
   return x;
 }
 
+// kWithhold (failure-path test only, stv_prefill_attn_timeout_test): the
+// producer issues no copy, so every wait on one runs out.
+template <bool kWithhold>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment of the operand tiles (the swizzle works on address bits).
@@ -152,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int u = unit_of(k, cta);
         if (u >= p.n_units) break;
         const Unit x = unit_info(p, u);
-        for (int i = 0; i < x.n_tiles; ++i) {
+        for (int i = 0; i < (kWithhold ? 0 : x.n_tiles); ++i) {
           const int st = g % kStages;
           if (!wait1(&bars->raw_empty[st], ((g / kStages) & 1) ^ 1, abort_flag)) {
             ok = false;
@@ -511,10 +514,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillParams& p, int grid, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+cudaError_t launch_prefill(const PrefillParams& p, int grid, cudaStream_t s, bool withhold_copies) {
+  auto kernel = withhold_copies ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(prefill_tc_kernel, grid, kThreads, kSmemBytes, s, p);
+  return launch_pdl(kernel, grid, kThreads, kSmemBytes, s, p);
 }
 
 }  // namespace stv

@@ -213,7 +213,8 @@ cudaError_t launch_quantize_q(const __half* q, int n_rows, int8_t* qi, float* sq
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);     // exact path; int4 cache (verify_tc.cu)
 cudaError_t launch_verify_i8(const VerifyParams& p, cudaStream_t s);  // int8 path, 3-bit cache (verify_i8.cu)
 cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t s);
-cudaError_t launch_prefill(const PrefillParams& p, int grid, cudaStream_t s);  // prefill_tc.cu
+// prefill_tc.cu; withhold_copies: failure-path test (every wait runs out)
+cudaError_t launch_prefill(const PrefillParams& p, int grid, cudaStream_t s, bool withhold_copies = false);
 cudaError_t launch_tree_accept(const int32_t* parent, const int32_t* draft, const int32_t* argmax, int T, int n_seqs,
                                int32_t* n_commit, int32_t* path, int32_t* out_ids, int32_t* status, cudaStream_t s);
 

@@ -115,6 +115,30 @@ def test_prefill_reports_bad_page(gpu):
     assert np.all(np.isfinite(gpu_prefill(shape, layer, seq, q, 200, "exact")))
 
 
+def test_prefill_timeout_reported_and_context_usable(gpu):
+    """Failure detection without a GPU fault: the persistent prefill kernel
+    with its copies withheld (stv_prefill_attn_timeout_test) has every
+    consumer's wait run out; the launch returns within seconds with
+    STV_DEV_TIMEOUT, and a normal prefill right after it matches the oracle.
+    The int8 path, which runs the chunked verify launches, refuses it."""
+    import time
+
+    shape, layer, seq, q, table, cache = prefill_case(200, 300, 24, 4, 23)
+    ws = torch.empty(stv.stv_prefill_workspace_bytes(shape, seq, 300), dtype=torch.uint8, device="cuda")
+    o = torch.empty((300, 24, 256), dtype=torch.float16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    stv.stv_prefill_attn_timeout_test(shape, layer, seq, q, 300, "exact", ws, o, dev_status=status)
+    torch.cuda.synchronize()
+    assert time.monotonic() - t0 < 30.0
+    assert int(status.item()) & stv.STV_DEV_TIMEOUT
+    with pytest.raises(stv.StvError) as e:
+        stv.stv_prefill_attn_timeout_test(shape, layer, seq, q, 300, "int8", ws, o)
+    assert e.value.status == stv.STV_ERR_UNIMPLEMENTED
+    check_prefill("exact", 200, 300, 24, 4)
+
+
 def test_prefill_deterministic_and_rejects_bad_args(gpu):
     shape, layer, seq, q, table, cache = prefill_case(100, 50, 24, 4, 9)
     a = gpu_prefill(shape, layer, seq, q, 50, "exact")
