@@ -58,6 +58,9 @@ constexpr int kSmemBytes = 1024 /*align slack*/ + (2 + kVBuffers) * kOperandByte
 // issues only after the softmax of tile i has arrived on p_full, so a slot is
 // never rewritten while it is read.
 constexpr int kKScaleSlots = 4;
+// Work units of at most this many tiles take the staged epilogue (measured at
+// T = 16: 14-tile units gain about 1 us per launch, 108-tile units lose 2 us).
+constexpr int kStagedEpilogueTiles = 48;
 template <int kFmt>
 struct Fmt {  // the 3-bit cache
   static constexpr int stages = kStages;
@@ -123,11 +126,49 @@ __device__ __forceinline__ bool settle(uint64_t* b, uint32_t parity, uint32_t pr
   return stv::settle<false>(b, parity, probed, abort_flag);
 }
 
+// The epilogue's copy of one softmax warp's 32 O rows (TMEM lane quarter
+// `quad`) into the workspace, staged through shared memory (`stage`: the
+// operand buffers, 128 KiB, free once every MMA has finished).  Each row goes
+// TMEM -> shared memory, its 16-byte pieces XOR-swizzled by row mod 8 so the
+// warp's stores spread over the banks; then the warp copies the rows out one
+// at a time, a lane per 16 bytes: coalesced 512-byte stores instead of 32
+// lanes writing 32 rows 1 KiB apart.  Out of line, so the tile loop's code
+// does not change with it.
+__device__ __noinline__ void epilogue_rows_staged(uint32_t lane_addr, uint8_t* stage, float* dst0, int quad, int R) {
+  const int lane = threadIdx.x & 31, r = quad * 32 + lane;
+  const uint32_t srow = su32(stage) + (uint32_t)r * 1024u;
+#pragma unroll 1
+  for (int chunk = 0; chunk < 8; ++chunk) {
+    uint32_t o[32];
+    tmem_ld32(lane_addr + kColO + 32 * chunk, o);
+    tmem_wait_ld(o);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      st_shared_v4(srow + chunk * 128u + (uint32_t)((j ^ (r & 7)) << 4), o[4 * j], o[4 * j + 1], o[4 * j + 2],
+                   o[4 * j + 3]);
+  }
+  __syncwarp();
+  const int r_end = min(R, quad * 32 + 32);
+#pragma unroll 1
+  for (int rr = quad * 32; rr < r_end; ++rr) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int q = lane + 32 * hf;  // 16-byte piece of the row, 0..63
+      const uint4 x = *reinterpret_cast<const uint4*>(stage + rr * 1024 + (q >> 3) * 128 + (((q & 7) ^ (rr & 7)) << 4));
+      reinterpret_cast<uint4*>(dst0 + (int64_t)rr * kHeadDim)[q] = x;
+    }
+  }
+}
+
 // kAppend: the round's tree rows are packed into the cache by this launch
 // (stv_append_verify_attn); the plain instantiation carries none of that code.
 // kWithhold (failure-path test only, stv_verify_attn_timeout_test): the
 // producer issues no copy, so every wait on one runs out.
-template <bool kAppend, int kFmt, bool kWithhold = false>
+// kStaged: the epilogue stages O through shared memory (launches whose work
+// units are short, where the epilogue is a large part of the launch; on long
+// units the out-of-line call's registers slow the tile loop more than the
+// coalesced stores save).
+template <bool kAppend, int kFmt, bool kWithhold = false, bool kStaged = false>
 __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_constant__ VerifyParams p) {
   using F = Fmt<kFmt>;
   constexpr bool kI4 = kFmt == kFmtInt4;    // one K scale per key, handed to the softmax
@@ -466,18 +507,22 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
     if (ok) ok = waitw(&bars->mma_done, 0, abort_flag);
     if (ok) {
       tc_after();
-      float* dst = p.o_part + ((int64_t)blockIdx.x * R + r) * kHeadDim;
+      if constexpr (kStaged) {
+        epilogue_rows_staged(lane_addr, kdeq0, p.o_part + (int64_t)blockIdx.x * R * kHeadDim, quad, R);
+      } else {
+        float* dst = p.o_part + ((int64_t)blockIdx.x * R + r) * kHeadDim;
 #pragma unroll 1
-      for (int chunk = 0; chunk < 8; ++chunk) {
-        uint32_t o[32];
-        tmem_ld32(lane_addr + kColO + 32 * chunk, o);
-        tmem_wait_ld(o);
-        if (r < R) {
+        for (int chunk = 0; chunk < 8; ++chunk) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + kColO + 32 * chunk, o);
+          tmem_wait_ld(o);
+          if (r < R) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            reinterpret_cast<float4*>(dst + 32 * chunk)[e] =
-                make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]), __uint_as_float(o[4 * e + 2]),
-                            __uint_as_float(o[4 * e + 3]));
+            for (int e = 0; e < 8; ++e)
+              reinterpret_cast<float4*>(dst + 32 * chunk)[e] =
+                  make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                              __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+          }
         }
       }
       if (r < R) {
@@ -749,9 +794,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
   if (tid == 0 && bars->abort) report(p.status, STV_DEV_TIMEOUT);
 }
 
-template <bool kAppend, int kFmt, bool kWithhold = false>
+template <bool kAppend, int kFmt, bool kWithhold = false, bool kStaged = false>
 cudaError_t launch_one(const VerifyParams& p, cudaStream_t s) {
-  auto kernel = verify_tc_kernel<kAppend, kFmt, kWithhold>;
+  auto kernel = verify_tc_kernel<kAppend, kFmt, kWithhold, kStaged>;
   constexpr int smem = Fmt<kFmt>::smem;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -769,7 +814,9 @@ cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s) {
   const bool append = p.k_tree != nullptr && p.v_tree != nullptr;
   if (p.fmt == kFmtInt4) return launch_one<false, kFmtInt4>(p, s);
   if (p.fmt == kFmtK4V2) return launch_one<false, kFmtK4V2>(p, s);
-  return append ? launch_one<true, kFmtBit3>(p, s) : launch_one<false, kFmtBit3>(p, s);
+  if (append) return launch_one<true, kFmtBit3>(p, s);
+  return p.tiles_per_split <= kStagedEpilogueTiles ? launch_one<false, kFmtBit3, false, true>(p, s)
+                                                    : launch_one<false, kFmtBit3>(p, s);
 }
 
 }  // namespace stv
