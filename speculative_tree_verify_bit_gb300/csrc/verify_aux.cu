@@ -54,15 +54,19 @@ cudaError_t launch_quantize_q(const __half* q, int n_rows, int8_t* qi, float* sq
 // a5: split_combine.  One warp per (sequence, KV head, row, 64-channel
 // quarter); lane = 2 channels.  Split kb + j's (m, l) sits in lane j of
 // chunk kb / 32.  The (m, l) of every split and the partial O of the first
-// two chunks of 32 splits are loaded together, one memory round trip for up
-// to 64 splits (later chunks take one more each); then M = max m, the
-// weights 2^(m - M), and the sums in split order, so the result does not
-// depend on timing.
+// kDepth splits are loaded together, one memory round trip for up to kDepth
+// splits (with kDepth = 64, later chunks of 32 take one more each); then
+// M = max m, the weights 2^(m - M), and the sums in split order, so the
+// result does not depend on timing, nor on kDepth.  kDepth is the smallest
+// of 16, 32, 64 that covers the launch's largest split count: the partials
+// in flight take 2 kDepth registers a lane, and a batch of short sequences
+// (many rows, few splits each) runs more warps per SM with fewer.
 
-// acc += the chunk's 32 partials weighted by w (lane j's weight is split j's)
-__device__ __forceinline__ void combine_chunk(const float2 (&o)[32], float w, float& acc0, float& acc1) {
+// acc += the chunk's N partials weighted by w (lane j's weight is split j's)
+template <int N>
+__device__ __forceinline__ void combine_chunk(const float2 (&o)[N], float w, float& acc0, float& acc1) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
+  for (int j = 0; j < N; ++j) {
     const float wk = __shfl_sync(0xffffffffu, w, j);
     // a split with weight 0 (no visible key for this row) adds nothing
     acc0 = wk != 0.f ? fmaf(wk, o[j].x, acc0) : acc0;
@@ -70,7 +74,9 @@ __device__ __forceinline__ void combine_chunk(const float2 (&o)[32], float w, fl
   }
 }
 
+template <int kDepth>
 __global__ void __launch_bounds__(256) split_combine_kernel(const __grid_constant__ CombineParams p) {
+  static_assert(kDepth == 16 || kDepth == 32 || kDepth == 64, "depth");
   grid_dep_wait();
   grid_dep_launch();
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -88,21 +94,25 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const __grid_constan
   const int64_t split_stride = (int64_t)p.R * kHeadDim;
   const float* src = p.o_part + (int64_t)u0 * split_stride + (int64_t)r * kHeadDim + quarter * 64 + lane * 2;
   // (m, l) of every split, 32 per register: at most kMaxChunks * 32 splits
-  constexpr int kMaxChunks = kMaxSplitsPerHead / 32;
+  // (kDepth <= 32: the launch has at most kDepth splits per head)
+  constexpr int kMaxChunks = kDepth == 64 ? kMaxSplitsPerHead / 32 : 1;
   float2 mlv[kMaxChunks];
 #pragma unroll
   for (int c = 0; c < kMaxChunks; ++c) {
     const int k = c * 32 + lane;
     mlv[c] = k < splits ? ml[(int64_t)(u0 + k) * p.R + r] : make_float2(-INFINITY, 0.f);
   }
-  // the partials of chunks 0 and 1, in flight with the (m, l) loads
-  float2 oa[32], ob[32];
+  // the first kDepth partials, in flight with the (m, l) loads
+  constexpr int kA = kDepth < 32 ? kDepth : 32;
+  float2 oa[kA], ob[kDepth == 64 ? 32 : 1];
 #pragma unroll
-  for (int j = 0; j < 32; ++j)
+  for (int j = 0; j < kA; ++j)
     oa[j] = j < splits ? *reinterpret_cast<const float2*>(src + j * split_stride) : make_float2(0.f, 0.f);
+  if constexpr (kDepth == 64) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j)
-    ob[j] = 32 + j < splits ? *reinterpret_cast<const float2*>(src + (32 + j) * split_stride) : make_float2(0.f, 0.f);
+    for (int j = 0; j < 32; ++j)
+      ob[j] = 32 + j < splits ? *reinterpret_cast<const float2*>(src + (32 + j) * split_stride) : make_float2(0.f, 0.f);
+  }
   float M = -INFINITY;
 #pragma unroll
   for (int c = 0; c < kMaxChunks; ++c) M = fmaxf(M, mlv[c].x);
@@ -114,19 +124,22 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const __grid_constan
     return w;
   };
   combine_chunk(oa, weight(mlv[0]), acc0, acc1);
-  if (splits > 32) combine_chunk(ob, weight(mlv[1]), acc0, acc1);
-  // chunks 2 and later (more than 64 splits: contexts past about 500K keys)
+  if constexpr (kDepth == 64) {
+    if (splits > 32) combine_chunk(ob, weight(mlv[1]), acc0, acc1);
+    // chunks 2 and later (more than 64 splits: contexts past about 500K keys)
 #pragma unroll 1
-  for (int c = 2; c < kMaxChunks && c * 32 < splits; ++c) {
-    float w = 0.f;
+    for (int c = 2; c < kMaxChunks && c * 32 < splits; ++c) {
+      float w = 0.f;
 #pragma unroll
-    for (int i = 2; i < kMaxChunks; ++i)
-      if (i == c) w = weight(mlv[i]);
-    const int n = min(32, splits - c * 32);
-    const float* sp = src + (int64_t)(c * 32) * split_stride;
+      for (int i = 2; i < kMaxChunks; ++i)
+        if (i == c) w = weight(mlv[i]);
+      const int n = min(32, splits - c * 32);
+      const float* sp = src + (int64_t)(c * 32) * split_stride;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) oa[j] = j < n ? *reinterpret_cast<const float2*>(sp + j * split_stride) : make_float2(0.f, 0.f);
-    combine_chunk(oa, w, acc0, acc1);
+      for (int j = 0; j < 32; ++j)
+        oa[j] = j < n ? *reinterpret_cast<const float2*>(sp + j * split_stride) : make_float2(0.f, 0.f);
+      combine_chunk(oa, w, acc0, acc1);
+    }
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
@@ -138,7 +151,12 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const __grid_constan
 
 cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t s) {
   const int warps = p.n_seqs * p.hkv * p.R * 4;  // four channel quarters per row
-  return launch_pdl(split_combine_kernel, (warps + 7) / 8, 256, 0, s, p);
+  int max_splits = 0;
+  for (int i = 0; i < p.n_seqs; ++i) max_splits = max(max_splits, p.seq[i].splits);
+  const int blocks = (warps + 7) / 8;
+  if (max_splits <= 16) return launch_pdl(split_combine_kernel<16>, blocks, 256, 0, s, p);
+  if (max_splits <= 32) return launch_pdl(split_combine_kernel<32>, blocks, 256, 0, s, p);
+  return launch_pdl(split_combine_kernel<64>, blocks, 256, 0, s, p);
 }
 
 // ---------------------------------------------------------------------------
