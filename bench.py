@@ -75,7 +75,8 @@ def verify_kernel_flops(ctx_list, t, hq=24):
 
 def launches_per_step(args, w: workloads.Workload) -> int:
     L = args.layers or w.layers
-    per_layer = (2 if args.fuse_append else 3) + (1 if args.path == "int8" else 0)
+    per_layer = (1 if args.one_launch and args.path == "exact" else 2 if args.fuse_append else 3) + \
+        (1 if args.path == "int8" else 0)
     return L * per_layer + 2
 
 
@@ -201,13 +202,14 @@ class GpuRound:
     """All layers of one workload resident on the GPU, plus one round's inputs."""
 
     def __init__(self, w: workloads.Workload, p_accept: float, device, layers: int | None = None,
-                 fuse_append: bool = False, group: int = 32, kv_format: int = 0):
+                 fuse_append: bool = False, group: int = 32, kv_format: int = 0, one_launch: bool = False):
         import torch
 
         import speculative_tree_verify_bit_gb300 as stv
 
         self.stv, self.torch, self.w, self.dev = stv, torch, w, device
         self.fuse_append = fuse_append
+        self.one_launch = one_launch  # exact path: append, verify and merge in one launch per layer
         self.L = layers or w.layers
         self.T, self.hq, self.hkv = w.t_nodes, w.hq, w.hkv
         self.shape = stv.make_shape(self.hq, self.hkv, group, kv_format)
@@ -241,7 +243,7 @@ class GpuRound:
             self.q.append(workloads.q_rows(seed, n, T, self.hq, device=device).contiguous())
         torch.cuda.synchronize()
         self.ws_bytes = stv.stv_verify_workspace_bytes(self.shape, self.seqs, T)
-        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=device)  # zero counters (one-launch layers)
         self.o = torch.empty((n, T, self.hq, 256), dtype=torch.float16, device=device)
         self.n_commit = torch.zeros(n, dtype=torch.int32, device=device)
         self.path = torch.zeros((n, T), dtype=torch.int32, device=device)
@@ -286,7 +288,17 @@ class GpuRound:
 
     def step(self, path, verify_events=None):
         stv = self.stv
+        one = self.one_launch and path == "exact"
         for l in range(self.L):
+            if one:  # append, verify and merge in one cooperative launch
+                if verify_events is not None:
+                    verify_events[l][0].record()
+                stv.stv_append_verify_combine(self.shape, self.layers[l], self.seqs, self.k_tree[l], self.v_tree[l],
+                                              self.q[l], self.parent, self.T, path, self.ws, self.o,
+                                              dev_status=self.status)
+                if verify_events is not None:
+                    verify_events[l][1].record()
+                continue
             if not self.fuse_append:
                 stv.stv_kv_append_pack(self.shape, self.layers[l], self.seqs, self.k_tree[l], self.v_tree[l],
                                        self.row_seq, self.row_pos, dev_status=self.status)
@@ -622,7 +634,8 @@ def run_gpu(args, rank, world):
     w = workloads.WORKLOADS[args.workload]
     p_accept = default_p_accept(args, w)
     r = GpuRound(w, p_accept, dev, layers=args.layers, fuse_append=args.fuse_append,
-                 group=KV_FORMATS[args.kv_format][0], kv_format=2 if args.kv_format == "k4v2" else 0)
+                 group=KV_FORMATS[args.kv_format][0], kv_format=2 if args.kv_format == "k4v2" else 0,
+                 one_launch=args.one_launch)
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -684,7 +697,7 @@ def run_gpu(args, rank, world):
         for name in ("tree32k", "ragged"):
             w2 = workloads.WORKLOADS[name]
             pa2 = w2.p_accept[0]
-            r2 = GpuRound(w2, pa2, dev)
+            r2 = GpuRound(w2, pa2, dev, one_launch=args.one_launch)
             rm, vm, ck = time_round(r2, args.path, n, 3, barrier, dev)
             configs[f"{name}/{args.path}/p{pa2:g}"] = config_line(w2, args.path, pa2, "bit3", rm, vm, ck, r2.L,
                                                                   int(r2.status.item()))
@@ -710,7 +723,7 @@ def run_gpu(args, rank, world):
 
 
 KERNEL_SOURCES = {  # the files a verify launch's code comes from, per path and cache format
-    "verify_tc": ("csrc/verify_tc.cu", "csrc/tc_util.cuh", "csrc/stv_device.cuh"),
+    "verify_tc": ("csrc/verify_tc.cu", "csrc/tc_util.cuh", "csrc/stv_device.cuh", "csrc/combine.cuh"),
     "verify_i8": ("csrc/verify_i8.cu", "csrc/tc_util.cuh", "csrc/stv_device.cuh"),
 }
 
@@ -791,7 +804,8 @@ def arm_config(args, w: workloads.Workload, p_accept: float, world: int) -> dict
             "hq": w.hq, "hkv": w.hkv, "head_dim": 256, "path": args.path, "p_accept": p_accept,
             "l2": "inputs larger than L2 (16 layers of packed KV)", "parallelism": f"replicas{world}",
             "timing": "median over steps of one CUDA-graph replay of the round, CUDA events",
-            "append": "fused into verify" if args.fuse_append else "separate launch",
+            "append": ("one launch per layer: append, verify and merge" if args.one_launch and args.path == "exact"
+                       else "fused into verify" if args.fuse_append else "separate launch"),
             "kv_format": {"bit3": "3-bit codes, fp16 scale per 32-group",
                           "int4": "int4 codes, fp16 scale per token and KV head",
                           "k4v2": "K 4-bit / V 2-bit codes, fp16 scale per 32-group"}[args.kv_format]}
@@ -841,6 +855,9 @@ def main():
     ap.add_argument("--fuse-append", action="store_true",
                     help="append the tree rows inside the verify launch (stv_append_verify_attn) instead of "
                          "with their own launch")
+    ap.add_argument("--one-launch", action="store_true",
+                    help="exact path: each layer's append, verify and merge in one cooperative launch "
+                         "(stv_append_verify_combine) instead of three")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kv-format", default="bit3", choices=sorted(KV_FORMATS),
                     help="cache format: the 3-bit cache (default), the int4 per-token-head cache or the "
@@ -858,6 +875,8 @@ def main():
     args.warmup = max(3, args.warmup)
     if args.fuse_append and args.kv_format != "bit3":
         ap.error("--fuse-append packs the 3-bit cache only")
+    if args.one_launch and (args.kv_format != "bit3" or args.fuse_append):
+        ap.error("--one-launch runs the 3-bit cache, without --fuse-append")
     if args.path == "int8" and args.kv_format == "k4v2":
         ap.error("the K 4 / V 2-bit cache runs the exact path only")
 

@@ -239,6 +239,43 @@ int stv_append_verify_attn(const stv_shape* shape, const stv_layer_cache* layer,
                            int path, void* workspace, size_t ws_bytes, int32_t* dev_status, stv_stream_t stream);
 
 /*
+ * a1 + a2..a4 + a5 in one launch: one layer of a verify round.  Packs the
+ * round's tree rows into the cache as stv_kv_append_pack would (row i of
+ * sequence s at position ctx_s + i), runs stv_verify_attn over the cache that
+ * now holds them, and merges the splits into o as stv_split_combine would
+ * ("elpis" README, "Why fast": tree verify pipe; Reddit posts (u/iamMess),
+ * second post: split-KV verify then merge; syv-ai README (mirror), CUDA graph
+ * notes: an uncaptured verify step is launch-bound).  The tree rows are
+ * packed by all work units together, (row, KV head) pairs dealt round-robin;
+ * a unit copies a tile holding tree keys once every pair is packed, and the
+ * units of each (sequence, KV head) merge their own partials once all of
+ * them have written theirs.  The units wait for one another (bounded), so
+ * the launch is cooperative: every unit resident at once.
+ *  k_tree, v_tree: device fp16 [n_seqs][T][hkv][256], read only.
+ *  q, parent, t_nodes: as stv_verify_attn; path: STV_PATH_EXACT only.
+ *  o: device fp16 [n_seqs][T][hq][256], the merged attention output.
+ *  workspace: as stv_verify_attn (the same size).  Its first
+ *   (2 + STV_MAX_SEQS * hkv) * 4 bytes, rounded up to 256, hold arrival
+ *   counters that must be zero before the first call on a workspace
+ *   (allocate it zero-filled).  Every call that completes leaves them zero,
+ *   and no other call writes them, whatever its plan; after STV_DEV_TIMEOUT
+ *   the caller zeroes them again.
+ * Cache bytes and o equal those of stv_kv_append_pack + stv_verify_attn +
+ * stv_split_combine on the same inputs, bit for bit.  On GB300 the three
+ * separate launches (in a CUDA graph) are faster: the packing warp's code
+ * slows the verify kernel's tile loop, and the merge's waits and dependent
+ * loads cost more than the merge launch they replace.
+ *  STV_ERR_INVALID_ARG when k_tree, v_tree or o is null;
+ *  STV_ERR_UNIMPLEMENTED for the int8 path and for the int4 and 4/2-bit caches;
+ *  STV_ERR_SHAPE_UNSUPPORTED when the split plan has more work units than the
+ *  device has SMs (more than sm_count / hkv sequences).
+ */
+int stv_append_verify_combine(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs, int n_seqs,
+                              const void* k_tree, const void* v_tree, const void* q, const int32_t* parent,
+                              int t_nodes, int path, void* workspace, size_t ws_bytes, void* o, int32_t* dev_status,
+                              stv_stream_t stream);
+
+/*
  * Failure-path test of stv_verify_attn (the pages have no counterpart: it
  * exists to test this library's failure detection without a GPU fault).
  * Same arguments and checks as stv_verify_attn, but the kernel's producer

@@ -49,7 +49,7 @@ EXPORTS = (
     "stv_verify_attn", "stv_split_combine", "stv_tree_accept", "stv_kv_commit", "stv_int8_qk_dots",
     "stv_verify_attn_no_alloc", "stv_append_verify_attn", "stv_lookup_workspace_bytes", "stv_lookup_draft",
     "stv_prefill_workspace_bytes", "stv_prefill_attn", "stv_verify_attn_timeout_test",
-    "stv_prefill_attn_timeout_test",
+    "stv_prefill_attn_timeout_test", "stv_append_verify_combine",
 )
 
 
@@ -117,6 +117,8 @@ def load() -> ctypes.CDLL:
         lib.stv_lookup_draft.argtypes = [P, I, I, I, I, P, P, P, P, P, ctypes.c_size_t, P]
         lib.stv_append_verify_attn.restype = I
         lib.stv_append_verify_attn.argtypes = [P, P, P, I, P, P, P, P, I, I, P, ctypes.c_size_t, P, P]
+        lib.stv_append_verify_combine.restype = I
+        lib.stv_append_verify_combine.argtypes = [P, P, P, I, P, P, P, P, I, I, P, ctypes.c_size_t, P, P, P]
         lib.stv_verify_attn_no_alloc.restype = I
         lib.stv_verify_attn_no_alloc.argtypes = [P, P, P, I, P, P, I, I, P, P, P]
         lib.stv_verify_attn_timeout_test.restype = I
@@ -275,6 +277,24 @@ def stv_append_verify_attn(shape, layer: LayerCache, seqs, k_tree, v_tree, q, pa
         _ptr(v_tree, torch.float16, "v_tree"), _ptr(q, torch.float16, "q"), _ptr(parent, torch.int32, "parent"),
         int(t_nodes), int(path), _ptr(workspace, name="workspace"), workspace.numel() * workspace.element_size(),
         _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
+
+
+def stv_append_verify_combine(shape, layer: LayerCache, seqs, k_tree, v_tree, q, parent, t_nodes: int, path,
+                              workspace, o, dev_status=None, stream=None):
+    """stv_kv_append_pack of the round's tree rows + stv_verify_attn +
+    stv_split_combine in one cooperative launch.  The workspace (the size
+    stv_verify_workspace_bytes gives) must be zero-filled before its first
+    use here; each completed call leaves its counters zero."""
+    import torch
+
+    lc = layer.c()
+    arr = _seq_array(seqs)
+    path = PATHS.get(path, path)
+    _check("stv_append_verify_combine", load().stv_append_verify_combine(
+        ctypes.byref(shape), ctypes.byref(lc), arr, len(seqs), _ptr(k_tree, torch.float16, "k_tree"),
+        _ptr(v_tree, torch.float16, "v_tree"), _ptr(q, torch.float16, "q"), _ptr(parent, torch.int32, "parent"),
+        int(t_nodes), int(path), _ptr(workspace, name="workspace"), workspace.numel() * workspace.element_size(),
+        _ptr(o, torch.float16, "o"), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream)))
 
 
 def stv_split_combine(shape, seqs, t_nodes: int, workspace, o, stream=None):

@@ -92,6 +92,11 @@ WsLayout ws_layout(const ShapeInfo& sh, int n_seqs, const Plan& plan) {
   WsLayout w;
   const size_t q_rows = (size_t)n_seqs * sh.T * sh.hq;
   size_t at = 0;
+  // stv_append_verify_combine's arrival counters: first, at a size fixed by
+  // the shape alone, so that calls with other plans on the same workspace
+  // never write over them
+  w.off_cnt = at;
+  at = align256(at + (size_t)(2 + STV_MAX_SEQS * sh.hkv) * sizeof(uint32_t));
   w.off_qi = at;
   at = align256(at + q_rows * kHeadDim);
   w.off_sq = at;
@@ -236,7 +241,7 @@ int stv_verify_workspace_bytes(const stv_shape* shape, const stv_seq* seqs, int 
 static int verify_common(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs, int n_seqs,
                          const void* k_tree, const void* v_tree, const void* q, const int32_t* parent, int t_nodes,
                          int path, void* workspace, size_t ws_bytes, int32_t* dev_status, stv_stream_t stream,
-                         int32_t* dots = nullptr, int withhold_copies = 0) {
+                         int32_t* dots = nullptr, int withhold_copies = 0, void* o_fused = nullptr) {
   ShapeInfo sh;
   int rc = check_shape(shape, t_nodes, &sh);
   if (rc) return rc;
@@ -244,10 +249,13 @@ static int verify_common(const stv_shape* shape, const stv_layer_cache* layer, c
   if (!q || !parent || !workspace || (path != STV_PATH_EXACT && path != STV_PATH_INT8)) return STV_ERR_INVALID_ARG;
   if (k_tree && sh.fmt != kFmtBit3) return STV_ERR_UNIMPLEMENTED;  // the fused append packs the 3-bit cache only
   if (path == STV_PATH_INT8 && sh.fmt == kFmtK4V2) return STV_ERR_UNIMPLEMENTED;  // exact path only on this cache
+  if (o_fused && (path != STV_PATH_EXACT || sh.fmt != kFmtBit3)) return STV_ERR_UNIMPLEMENTED;
   int sm = 0;
   if ((rc = device_sm_count(&sm))) return rc;
   Plan plan;
   if ((rc = make_plan(sh, seqs, n_seqs, sm, &plan))) return rc;
+  // the fused launch's units wait for one another: all of them resident at once
+  if (o_fused && plan.n_units > sm) return STV_ERR_SHAPE_UNSUPPORTED;
   const WsLayout wl = ws_layout(sh, n_seqs, plan);
   if (ws_bytes < wl.total) return STV_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -278,6 +286,12 @@ static int verify_common(const stv_shape* shape, const stv_layer_cache* layer, c
   p.dots = dots;
   p.test_withhold_copies = withhold_copies;
   p.status = dev_status;
+  if (o_fused) {
+    p.o_out = static_cast<__half*>(o_fused);
+    p.cnt = reinterpret_cast<uint32_t*>(ws + wl.off_cnt);
+    p.n_pairs = n_seqs * sh.T * sh.hkv;
+    p.packed_target = std::min(p.n_units, p.n_pairs);  // one packing warp per unit that has a pair
+  }
   cudaStream_t s = (cudaStream_t)stream;
   if (path == STV_PATH_INT8) {
     cudaError_t e = launch_quantize_q(p.q, n_seqs * sh.T * sh.hq, reinterpret_cast<int8_t*>(ws + wl.off_qi),
@@ -300,6 +314,15 @@ int stv_append_verify_attn(const stv_shape* shape, const stv_layer_cache* layer,
   if (!k_tree || !v_tree) return STV_ERR_INVALID_ARG;
   return verify_common(shape, layer, seqs, n_seqs, k_tree, v_tree, q, parent, t_nodes, path, workspace, ws_bytes,
                        dev_status, stream);
+}
+
+int stv_append_verify_combine(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs, int n_seqs,
+                              const void* k_tree, const void* v_tree, const void* q, const int32_t* parent,
+                              int t_nodes, int path, void* workspace, size_t ws_bytes, void* o, int32_t* dev_status,
+                              stv_stream_t stream) {
+  if (!k_tree || !v_tree || !o) return STV_ERR_INVALID_ARG;
+  return verify_common(shape, layer, seqs, n_seqs, k_tree, v_tree, q, parent, t_nodes, path, workspace, ws_bytes,
+                       dev_status, stream, nullptr, 0, o);
 }
 
 int stv_verify_attn_timeout_test(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs,

@@ -78,7 +78,7 @@ struct Plan {
 
 // Workspace carve-up (byte offsets, each 256-aligned).
 struct WsLayout {
-  size_t off_qi, off_sq, off_opart, off_ml, total;
+  size_t off_qi, off_sq, off_opart, off_ml, off_cnt, total;
 };
 
 // Cache formats (include/stv.h): the pages' 3-bit cache, the int4
@@ -120,6 +120,16 @@ struct VerifyParams {
   // copy, every wait on one runs out and the kernel reports STV_DEV_TIMEOUT.
   int test_withhold_copies;
   int32_t* status;
+  // One launch per layer (stv_append_verify_combine), or null: the round's
+  // tree rows (k_tree, v_tree) are packed by every work unit, (row, KV head)
+  // pair q = (s * T + i) * hkv + h by unit q mod n_units, and the units then
+  // merge the splits into o_out, the items dealt over the whole launch.
+  // cnt (workspace, zero between launches): [0] packing warps done, [1] units
+  // done, [2 + s * hkv + h] units of (s, h) whose partials are written.
+  __half* o_out;
+  uint32_t* cnt;
+  int n_pairs;
+  int packed_target;  // packing warps that arrive: min(n_units, n_pairs)
 };
 
 // Parameters of one prefill launch (prefill_tc.cu, exact path, 3-bit cache):
@@ -196,6 +206,28 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t sme
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e != cudaSuccess) (void)cudaGetLastError();
+  return e;
+}
+
+// The same launch, cooperative as well: every CTA of the grid is resident at
+// once, so CTAs of the launch may wait (bounded) for one another.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_coop(void (*kernel)(KArgs...), int grid, int block, size_t smem, cudaStream_t s,
+                            Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
   if (e != cudaSuccess) (void)cudaGetLastError();
   return e;

@@ -94,6 +94,28 @@ __device__ __forceinline__ bool settle(uint64_t* b, uint32_t parity, uint32_t pr
   return waitw<kPoll>(b, parity, abort_flag);
 }
 
+// Bounded wait, by one thread, until a device-memory counter that other CTAs
+// of the same launch increment reaches `target`.  The load is an acquire, so
+// what those CTAs wrote before their increments is visible afterwards; the
+// proxy fence then orders it before this thread's later bulk copies.  The
+// CTAs waited for must be resident (a cooperative launch).  False on timeout
+// (about 1 s; sets the CTA's abort flag) or when the CTA aborted.
+constexpr uint32_t kCountWaitLimit = 1u << 20;
+__device__ __forceinline__ bool wait_count(const uint32_t* c, uint32_t target, volatile int* abort_flag) {
+  for (uint32_t it = 0; it < kCountWaitLimit; ++it) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+    if (v >= target) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      return true;
+    }
+    if ((it & 63) == 63 && *abort_flag) return false;
+    __nanosleep(1000);
+  }
+  *abort_flag = 1;
+  return false;
+}
+
 // ---- copies and proxies ----
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(

@@ -35,6 +35,7 @@
 // exceeds it by more than 2^8, so P <= 256 in fp16 and O rescales are rare.
 // Every wait is bounded; a timeout sets a CTA abort flag, every role stops,
 // in-flight copies and MMAs are waited for (bounded) and TMEM is freed.
+#include "combine.cuh"
 #include "stv_device.cuh"
 #include "tc_util.cuh"
 
@@ -160,6 +161,86 @@ __device__ __noinline__ void epilogue_rows_staged(uint32_t lane_addr, uint8_t* s
   }
 }
 
+// kFused: the round's tree rows (a1), packed by one extra warp of each unit
+// before the tiles are read: (sequence, row, KV head) pair q goes to unit
+// q mod n_units; lane = channel of each 32-channel group in turn, V bits by
+// atomics (rows packed by other units may share a V word).  A warp that
+// packed arrives once on the launch's counter, after a proxy fence and a
+// release.  Out of line, so that none of it enters the other roles' code.
+__device__ __noinline__ void fused_pack_tree_rows(const VerifyParams& p) {
+  const int lane = threadIdx.x & 31;
+  bool packed = false;
+  for (int q = blockIdx.x; q < p.n_pairs; q += p.n_units) {
+    const int h2 = q % p.hkv, si = q / p.hkv, s2 = si / p.T;
+    const int64_t pos = (int64_t)p.seq[s2].ctx + si % p.T;
+    const int64_t row = ((int64_t)si * p.hkv + h2) * kHeadDim;
+    uint8_t* hb = const_cast<uint8_t*>(
+        head_block(p.seq[s2], p.pool, p.page_bytes, p.pool_pages, pos, h2, lane == 0 ? p.status : nullptr));
+    if (hb) {
+#pragma unroll 1
+      for (int g = 0; g < 8; ++g)
+        append_row_channel(__half2float(p.k_tree[row + g * 32 + lane]), __half2float(p.v_tree[row + g * 32 + lane]),
+                           hb, (int)(pos & (kPageTok - 1)), g * 32 + lane);
+    }
+    packed = true;
+  }
+  if (packed) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence();
+      atomicAdd(p.cnt, 1u);
+    }
+  }
+}
+
+// kFused: a5 inside the verify launch, by every warp of a unit after its
+// teardown.  The unit first publishes its partials on its (sequence, KV
+// head)'s counter (the softmax warps wrote them before the teardown barrier;
+// the release is cumulative over them).  The merge's items, (sequence, KV
+// head, row, channel quarter) over the whole launch, are dealt to the units
+// in equal contiguous ranges; a warp waits (bounded: the launch is
+// cooperative, every unit is resident) until every unit of an item's head has
+// published, then merges it with combine_row_quarter_lean (loads from L2),
+// whose sums are split_combine's, bit for bit.  A unit that aborted still
+// publishes and counts itself done, so no other unit waits for it past its
+// bound.  The last unit of the launch to be done zeroes the counters for the
+// next launch: every unit has passed every wait of this one by then.
+__device__ __noinline__ void fused_merge(const VerifyParams& p, volatile int* abort_flag, int my_s, int my_h) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, n_warps = blockDim.x >> 5;
+  if (tid == 0) {
+    __threadfence();
+    atomicAdd(p.cnt + 2 + my_s * p.hkv + my_h, 1u);
+  }
+  const int per_head = 4 * p.R, n_items = p.n_seqs * p.hkv * per_head;
+  const int i0 = (int)((int64_t)blockIdx.x * n_items / p.n_units);
+  const int i1 = (int)((int64_t)(blockIdx.x + 1) * n_items / p.n_units);
+  int waited = -1;
+  bool ok = !*abort_flag;
+  for (int it = i0 + warp; ok && it < i1; it += n_warps) {
+    const int head = it / per_head, rq = it % per_head;
+    const int s = head / p.hkv, h = head % p.hkv;
+    if (head != waited) {
+      bool w = true;
+      if (lane == 0) w = wait_count(p.cnt + 2 + head, (uint32_t)p.seq[s].splits, abort_flag);
+      ok = __shfl_sync(0xffffffffu, w, 0);
+      waited = head;
+      if (!ok) break;
+    }
+    combine_row_quarter_lean<true>(p.seq[s], s, h, rq >> 2, rq & 3, p.R, p.T, p.hq, p.G, p.o_part, p.ml, p.o_out);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(p.cnt + 1, 1u) == (uint32_t)p.n_units - 1) {
+      p.cnt[0] = 0u;
+      p.cnt[1] = 0u;
+      for (int i = 0; i < p.n_seqs * p.hkv; ++i) p.cnt[2 + i] = 0u;
+      __threadfence();
+    }
+  }
+}
+
 // kAppend: the round's tree rows are packed into the cache by this launch
 // (stv_append_verify_attn); the plain instantiation carries none of that code.
 // kWithhold (failure-path test only, stv_verify_attn_timeout_test): the
@@ -168,8 +249,14 @@ __device__ __noinline__ void epilogue_rows_staged(uint32_t lane_addr, uint8_t* s
 // units are short, where the epilogue is a large part of the launch; on long
 // units the out-of-line call's registers slow the tile loop more than the
 // coalesced stores save).
-template <bool kAppend, int kFmt, bool kWithhold = false, bool kStaged = false>
-__global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_constant__ VerifyParams p) {
+// kFused: one launch per layer (stv_append_verify_combine, cooperative): a
+// fifteenth warp packs the round's tree rows (fused_pack_tree_rows), a unit
+// copies a tile holding tree keys once every packing warp of the launch has
+// arrived on a device counter, and after the teardown the units merge the
+// splits (fused_merge).
+template <bool kAppend, int kFmt, bool kWithhold = false, bool kStaged = false, bool kFused = false>
+__global__ void __launch_bounds__(kFused ? kThreads + 32 : kThreads, 1)
+    verify_tc_kernel(const __grid_constant__ VerifyParams p) {
   using F = Fmt<kFmt>;
   constexpr bool kI4 = kFmt == kFmtInt4;    // one K scale per key, handed to the softmax
   constexpr bool kKv2 = kFmt == kFmtK4V2;  // 4-bit K, 2-bit V, scales per 32-channel group
@@ -251,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
     // =================== producer ===================
     if (lane == 0) {
       int issued = 0;
-      bool tree_ready = !kAppend;
+      bool tree_ready = !kAppend && !kFused;
       for (int i = 0; i < (kWithhold ? 0 : n_tiles); ++i) {
         const int st = i % F::stages;
         if (!wait1(&bars->raw_empty[st], ((i / F::stages) & 1) ^ 1, abort_flag)) break;
@@ -259,7 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
         // a tile holding tree keys is copied only after the unpack warps have
         // packed them (their global writes are fenced for the async proxy)
         if (!tree_ready && key0 + kTileTok > sd.ctx && key0 < sd.ctx + T) {
-          if (!wait1(&bars->tree_packed, 0, abort_flag)) break;
+          if constexpr (kFused) {
+            if (!wait_count(p.cnt, (uint32_t)p.packed_target, abort_flag)) break;
+          } else {
+            if (!wait1(&bars->tree_packed, 0, abort_flag)) break;
+          }
           tree_ready = true;
         }
         const int64_t lp = key0 >> 8;
@@ -530,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
         p.ml[((int64_t)blockIdx.x * R + r) * 2 + 1] = l;
       }
     }
-  } else {
+  } else if (warp < 14) {
     // =================== unpack (256 threads) ===================
     const int ut = tid - 6 * 32;
     // K: key and 64-channel column block.  Each group of 8 consecutive lanes
@@ -782,6 +873,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
         mbar_arrive(&bars->raw_empty[st]);
       }
     }
+  } else {
+    // =================== kFused: the tree rows' packing warp ===================
+    if constexpr (kFused) fused_pack_tree_rows(p);
   }
 
   // ---- teardown ----
@@ -791,16 +885,18 @@ __global__ void __launch_bounds__(kThreads, 1) verify_tc_kernel(const __grid_con
     tc_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
+  if constexpr (kFused) fused_merge(p, abort_flag, s, h);
   if (tid == 0 && bars->abort) report(p.status, STV_DEV_TIMEOUT);
 }
 
-template <bool kAppend, int kFmt, bool kWithhold = false, bool kStaged = false>
+template <bool kAppend, int kFmt, bool kWithhold = false, bool kStaged = false, bool kFused = false>
 cudaError_t launch_one(const VerifyParams& p, cudaStream_t s) {
-  auto kernel = verify_tc_kernel<kAppend, kFmt, kWithhold, kStaged>;
+  auto kernel = verify_tc_kernel<kAppend, kFmt, kWithhold, kStaged, kFused>;
   constexpr int smem = Fmt<kFmt>::smem;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kernel, p.n_units, kThreads, smem, s, p);
+  if constexpr (kFused) return launch_pdl_coop(kernel, p.n_units, kThreads + 32, smem, s, p);
+  else return launch_pdl(kernel, p.n_units, kThreads, smem, s, p);
 }
 
 }  // namespace
@@ -808,6 +904,10 @@ cudaError_t launch_one(const VerifyParams& p, cudaStream_t s) {
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s) {
   // the int8 path on the 3-bit cache forms per-group integer dots: its own kernel
   if (p.path == STV_PATH_INT8 && p.fmt == kFmtBit3) return launch_verify_i8(p, s);
+  // one launch per layer: append, verify and merge (exact path, 3-bit cache)
+  if (p.o_out)
+    return p.tiles_per_split <= kStagedEpilogueTiles ? launch_one<false, kFmtBit3, false, true, true>(p, s)
+                                                      : launch_one<false, kFmtBit3, false, false, true>(p, s);
   if (p.test_withhold_copies)
     return p.fmt == kFmtInt4 ? launch_one<false, kFmtInt4, true>(p, s) : launch_one<false, kFmtBit3, true>(p, s);
   // the fused append packs the 3-bit cache only (the host refuses it for the others)

@@ -72,8 +72,9 @@ def test_workspace_bytes_long_context_plan(lib):
     sq = 16 * 24 * 4
     opart = 152 * 96 * 256 * 4
     ml = 152 * 96 * 2 * 4
+    cnt = (2 + 64 * 4) * 4  # stv_append_verify_combine's counters, first: 2 + STV_MAX_SEQS * hkv words
     a = lambda x: (x + 255) // 256 * 256
-    assert nbytes == a(a(a(qi) + sq) + opart) + ml
+    assert nbytes == a(a(a(a(cnt) + qi) + sq) + opart) + ml
 
 
 def test_workspace_units_never_exceed_sm_count(lib):
@@ -95,7 +96,8 @@ def test_split_plan_caps_splits_per_head(lib):
     units = 4 * -(-16385 // 65)
     a = lambda x: (x + 255) // 256 * 256
     assert units == 1012
-    assert nbytes == a(a(a(16 * 24 * 256) + 16 * 24 * 4) + units * 96 * 256 * 4) + units * 96 * 2 * 4
+    cnt = (2 + 64 * 4) * 4
+    assert nbytes == a(a(a(a(cnt) + 16 * 24 * 256) + 16 * 24 * 4) + units * 96 * 256 * 4) + units * 96 * 2 * 4
 
 
 @pytest.mark.parametrize("ctxs,pages,t,rc", [
