@@ -191,8 +191,11 @@ int stv_kv_append_pack(const stv_shape* shape, const stv_layer_cache* layer, con
  * sm_count: SMs the split plan targets; 0 = the current device's count
  * (stv_verify_attn and stv_split_combine always plan for the current device).
  * The plan cuts each (sequence, KV head) key range into splits of equal
- * whole 64-key tiles: as many work units as SMs at most, and never more
- * than 256 splits for one (sequence, KV head).
+ * whole 64-key tiles, never more than 256 splits for one (sequence, KV
+ * head): as many work units as SMs at most; or, for several sequences on the
+ * 3-bit cache, the split whose work units, dealt longest first to the SMs by
+ * the persistent verify kernel, finish first (up to 640 units, 24 MiB of
+ * partials), so that a batch of unequal sequences keeps every SM busy.
  */
 int stv_verify_workspace_bytes(const stv_shape* shape, const stv_seq* seqs, int n_seqs, int t_nodes, int sm_count,
                                size_t* bytes);

@@ -57,7 +57,75 @@ static int device_sm_count(int* n) {
   return STV_OK;
 }
 
-int make_plan(const ShapeInfo& sh, const stv_seq* seqs, int n_seqs, int sm_count, Plan* plan) {
+// The persistent verify kernel's deal for split k: units longest first (the
+// full units of k tiles in unit order, then each sequence's last, shorter
+// units, longest first), CTA b taking the b-th, then the (2n - 1 - b)-th,
+// ... (snake order over n = min(SMs, units) CTAs).  Returns the makespan in
+// tiles, each unit costing its tiles plus kUnitCostTiles (its epilogue and
+// the next unit's Q load, about three tiles' time), or -1 past
+// kMaxPersistUnits units; fills `order` (unit numbers, sequence-major, then
+// KV head, then split) when given.
+constexpr int kUnitCostTiles = 3;
+static int64_t balanced_deal(const int64_t* tiles, int n_seqs, int hkv, int64_t k, int sm, int16_t* order) {
+  int sp[STV_MAX_SEQS], rem[STV_MAX_SEQS], by_rem[STV_MAX_SEQS], base[STV_MAX_SEQS];
+  int n = 0;
+  for (int s = 0; s < n_seqs; ++s) {
+    sp[s] = (int)((tiles[s] + k - 1) / k);
+    rem[s] = (int)(tiles[s] - (int64_t)(sp[s] - 1) * k);
+    base[s] = n;
+    n += hkv * sp[s];
+    by_rem[s] = s;
+  }
+  if (n > kMaxPersistUnits) return -1;
+  // sequences by their last unit's length, longest first (ties: lower index)
+  for (int i = 1; i < n_seqs; ++i)
+    for (int j = i; j > 0 && rem[by_rem[j]] > rem[by_rem[j - 1]]; --j) std::swap(by_rem[j], by_rem[j - 1]);
+  const int ctas = std::min(sm, n);
+  int64_t load[kMaxPersistUnits];
+  for (int b = 0; b < ctas; ++b) load[b] = 0;
+  int w = 0;
+  auto deal = [&](int unit, int len) {
+    const int kk = w / ctas, b = w % ctas;
+    load[(kk & 1) ? ctas - 1 - b : b] += len + kUnitCostTiles;
+    if (order) order[w] = (int16_t)unit;
+    ++w;
+  };
+  for (int s = 0; s < n_seqs; ++s)  // full units (a last unit of k tiles is one too)
+    for (int h = 0; h < hkv; ++h)
+      for (int j = 0; j < sp[s]; ++j)
+        if (j + 1 < sp[s] || rem[s] == k) deal(base[s] + h * sp[s] + j, (int)k);
+  for (int i = 0; i < n_seqs; ++i) {
+    const int s = by_rem[i];
+    if (rem[s] == k) continue;
+    for (int h = 0; h < hkv; ++h) deal(base[s] + h * sp[s] + sp[s] - 1, rem[s]);
+  }
+  int64_t most = 0;
+  for (int b = 0; b < ctas; ++b) most = std::max(most, load[b]);
+  return most;
+}
+
+// The last balanced plan this thread made, and what it was made for (a
+// verify round's calls -- workspace size, verify, merge, for every layer --
+// ask for the same plan).
+struct PlanMemo {
+  bool valid = false;
+  int hkv, T, R, fmt, sm, n_seqs;
+  int32_t ctx[STV_MAX_SEQS];
+  Plan plan;
+};
+
+int make_plan(const ShapeInfo& sh, const stv_seq* seqs, int n_seqs, int sm_count, Plan* plan, bool balance) {
+  balance = balance && n_seqs > 1 && sh.fmt == kFmtBit3;
+  static thread_local PlanMemo memo;
+  if (balance && memo.valid && memo.hkv == sh.hkv && memo.T == sh.T && memo.R == sh.R && memo.fmt == sh.fmt &&
+      memo.sm == sm_count && memo.n_seqs == n_seqs) {
+    bool same = true;
+    for (int s = 0; s < n_seqs && same; ++s) same = memo.ctx[s] == seqs[s].ctx;
+    if (same) {
+      *plan = memo.plan;
+      return STV_OK;
+    }
+  }
   int64_t tiles[STV_MAX_SEQS], total = 0;
   for (int s = 0; s < n_seqs; ++s) {
     tiles[s] = ((int64_t)seqs[s].ctx + sh.T + kTileTok - 1) / kTileTok;
@@ -66,13 +134,38 @@ int make_plan(const ShapeInfo& sh, const stv_seq* seqs, int n_seqs, int sm_count
   const int64_t target = sm_count > 0 ? sm_count : 1;
   int64_t k = (total + target - 1) / target;
   if (k < 1) k = 1;
-  for (int s = 0; s < n_seqs; ++s)  // at most kMaxSplitsPerHead splits per (sequence, KV head)
-    k = std::max<int64_t>(k, (tiles[s] + kMaxSplitsPerHead - 1) / kMaxSplitsPerHead);
+  int64_t k_min = 1;  // at most kMaxSplitsPerHead splits per (sequence, KV head)
+  for (int s = 0; s < n_seqs; ++s)
+    k_min = std::max<int64_t>(k_min, (tiles[s] + kMaxSplitsPerHead - 1) / kMaxSplitsPerHead);
+  k = std::max(k, k_min);
   for (;;) {
     int64_t units = 0;
     for (int s = 0; s < n_seqs; ++s) units += sh.hkv * ((tiles[s] + k - 1) / k);
     if (units <= target || units <= (int64_t)n_seqs * sh.hkv) break;
     ++k;
+  }
+  // One unit per SM, as above, leaves a batch of unequal sequences waiting
+  // for its longest units (each sequence's split count rounds up).  For
+  // several sequences on the 3-bit cache, the persistent kernel may take
+  // more units than SMs: choose the split whose deal finishes first (ties to
+  // the larger split), within kMaxPersistUnits units and 24 MiB of partials.
+  plan->persist_ctas = 0;
+  if (balance) {
+    int64_t best = balanced_deal(tiles, n_seqs, sh.hkv, k, (int)target, nullptr), best_k = k;
+    if (best >= 0) {
+      for (int64_t kc = k - 1; kc >= std::max(k_min, k / 4); --kc) {
+        int64_t units = 0;
+        for (int s = 0; s < n_seqs; ++s) units += sh.hkv * ((tiles[s] + kc - 1) / kc);
+        if (units > kMaxPersistUnits || units * sh.R * kHeadDim * (int64_t)sizeof(float) > ((int64_t)24 << 20)) break;
+        const int64_t cost = balanced_deal(tiles, n_seqs, sh.hkv, kc, (int)target, nullptr);
+        if (cost >= 0 && cost < best) {
+          best = cost;
+          best_k = kc;
+        }
+      }
+      k = best_k;
+      balanced_deal(tiles, n_seqs, sh.hkv, k, (int)target, plan->order);
+    }
   }
   plan->tiles_per_split = (int)k;
   int base = 0;
@@ -83,6 +176,18 @@ int make_plan(const ShapeInfo& sh, const stv_seq* seqs, int n_seqs, int sm_count
   }
   plan->unit_base[n_seqs] = base;
   plan->n_units = base;
+  if (balance && base <= kMaxPersistUnits) plan->persist_ctas = (int)std::min<int64_t>(target, base);
+  if (balance) {
+    memo.valid = true;
+    memo.hkv = sh.hkv;
+    memo.T = sh.T;
+    memo.R = sh.R;
+    memo.fmt = sh.fmt;
+    memo.sm = sm_count;
+    memo.n_seqs = n_seqs;
+    for (int s = 0; s < n_seqs; ++s) memo.ctx[s] = seqs[s].ctx;
+    memo.plan = *plan;
+  }
   return STV_OK;
 }
 
@@ -223,8 +328,8 @@ int stv_kv_append_pack(const stv_shape* shape, const stv_layer_cache* layer, con
   return to_status(launch_kv_append(p, (cudaStream_t)stream));
 }
 
-int stv_verify_workspace_bytes(const stv_shape* shape, const stv_seq* seqs, int n_seqs, int t_nodes, int sm_count,
-                               size_t* bytes) {
+static int workspace_bytes(const stv_shape* shape, const stv_seq* seqs, int n_seqs, int t_nodes, int sm_count,
+                           size_t* bytes, bool balance) {
   ShapeInfo sh;
   int rc = check_shape(shape, t_nodes, &sh);
   if (rc) return rc;
@@ -232,16 +337,26 @@ int stv_verify_workspace_bytes(const stv_shape* shape, const stv_seq* seqs, int 
   if (!bytes || sm_count < 0) return STV_ERR_INVALID_ARG;
   if (sm_count == 0 && (rc = device_sm_count(&sm_count))) return rc;
   Plan plan;
-  if ((rc = make_plan(sh, seqs, n_seqs, sm_count, &plan))) return rc;
+  if ((rc = make_plan(sh, seqs, n_seqs, sm_count, &plan, balance))) return rc;
   *bytes = ws_layout(sh, n_seqs, plan).total;
   return STV_OK;
 }
 
+int stv_verify_workspace_bytes(const stv_shape* shape, const stv_seq* seqs, int n_seqs, int t_nodes, int sm_count,
+                               size_t* bytes) {
+  return workspace_bytes(shape, seqs, n_seqs, t_nodes, sm_count, bytes, true);
+}
+
 // stv_verify_attn, and stv_append_verify_attn when k_tree / v_tree are given.
+// balance: the split plan the public calls share (stv_verify_workspace_bytes,
+// stv_split_combine); the library's own launch sequences (chunked prefill)
+// use the one-unit-per-SM plan, and so does the one-launch layer, whose
+// units wait for one another.
 static int verify_common(const stv_shape* shape, const stv_layer_cache* layer, const stv_seq* seqs, int n_seqs,
                          const void* k_tree, const void* v_tree, const void* q, const int32_t* parent, int t_nodes,
                          int path, void* workspace, size_t ws_bytes, int32_t* dev_status, stv_stream_t stream,
-                         int32_t* dots = nullptr, int withhold_copies = 0, void* o_fused = nullptr) {
+                         int32_t* dots = nullptr, int withhold_copies = 0, void* o_fused = nullptr,
+                         bool balance = true) {
   ShapeInfo sh;
   int rc = check_shape(shape, t_nodes, &sh);
   if (rc) return rc;
@@ -253,7 +368,7 @@ static int verify_common(const stv_shape* shape, const stv_layer_cache* layer, c
   int sm = 0;
   if ((rc = device_sm_count(&sm))) return rc;
   Plan plan;
-  if ((rc = make_plan(sh, seqs, n_seqs, sm, &plan))) return rc;
+  if ((rc = make_plan(sh, seqs, n_seqs, sm, &plan, balance && !o_fused))) return rc;
   // the fused launch's units wait for one another: all of them resident at once
   if (o_fused && plan.n_units > sm) return STV_ERR_SHAPE_UNSUPPORTED;
   const WsLayout wl = ws_layout(sh, n_seqs, plan);
@@ -286,6 +401,12 @@ static int verify_common(const stv_shape* shape, const stv_layer_cache* layer, c
   p.dots = dots;
   p.test_withhold_copies = withhold_copies;
   p.status = dev_status;
+  // the persistent kernel runs the exact path on the 3-bit cache (no fused
+  // append, no inspection, no failure-path test)
+  if (plan.persist_ctas > 0 && path == STV_PATH_EXACT && sh.fmt == kFmtBit3 && !k_tree && !dots && !withhold_copies) {
+    p.persist_ctas = plan.persist_ctas;
+    memcpy(p.order, plan.order, sizeof(int16_t) * plan.n_units);
+  }
   if (o_fused) {
     p.o_out = static_cast<__half*>(o_fused);
     p.cnt = reinterpret_cast<uint32_t*>(ws + wl.off_cnt);
@@ -332,8 +453,8 @@ int stv_verify_attn_timeout_test(const stv_shape* shape, const stv_layer_cache* 
                        dev_status, stream, nullptr, 1);
 }
 
-int stv_split_combine(const stv_shape* shape, const stv_seq* seqs, int n_seqs, int t_nodes, const void* workspace,
-                      size_t ws_bytes, void* o, stv_stream_t stream) {
+static int combine_common(const stv_shape* shape, const stv_seq* seqs, int n_seqs, int t_nodes, const void* workspace,
+                          size_t ws_bytes, void* o, stv_stream_t stream, bool balance) {
   ShapeInfo sh;
   int rc = check_shape(shape, t_nodes, &sh);
   if (rc) return rc;
@@ -342,7 +463,7 @@ int stv_split_combine(const stv_shape* shape, const stv_seq* seqs, int n_seqs, i
   int sm = 0;
   if ((rc = device_sm_count(&sm))) return rc;
   Plan plan;
-  if ((rc = make_plan(sh, seqs, n_seqs, sm, &plan))) return rc;
+  if ((rc = make_plan(sh, seqs, n_seqs, sm, &plan, balance))) return rc;
   const WsLayout wl = ws_layout(sh, n_seqs, plan);
   if (ws_bytes < wl.total) return STV_ERR_WORKSPACE_TOO_SMALL;
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
@@ -361,6 +482,11 @@ int stv_split_combine(const stv_shape* shape, const stv_seq* seqs, int n_seqs, i
   return to_status(launch_split_combine(p, (cudaStream_t)stream));
 }
 
+int stv_split_combine(const stv_shape* shape, const stv_seq* seqs, int n_seqs, int t_nodes, const void* workspace,
+                      size_t ws_bytes, void* o, stv_stream_t stream) {
+  return combine_common(shape, seqs, n_seqs, t_nodes, workspace, ws_bytes, o, stream, true);
+}
+
 // ---------------------------------------------------------------------------
 // Prefill (next row f2): chunks of C prompt tokens as chain trees, up to
 // STV_MAX_SEQS chunks per verify launch, then the split merge.
@@ -376,8 +502,8 @@ int stv_prefill_workspace_bytes(const stv_shape* shape, const stv_seq* seq, int 
   rc = for_each_prefill_launch(n_tokens, c, [&](const PrefillLaunch& pl) -> int {
     stv_seq seqs[STV_MAX_SEQS];
     prefill_seqs(seq, pl, seqs);
-    size_t b = 0;
-    if (int r = stv_verify_workspace_bytes(shape, seqs, pl.count, pl.t, 0, &b)) return r;
+    size_t b = 0;  // the chunk launches use the one-unit-per-SM plan
+    if (int r = workspace_bytes(shape, seqs, pl.count, pl.t, 0, &b, false)) return r;
     most = b > most ? b : most;
     return (int)STV_OK;
   });
@@ -439,9 +565,11 @@ static int prefill_common(const stv_shape* shape, const stv_layer_cache* layer, 
     const __half* qs = static_cast<const __half*>(q) + (size_t)pl.start * row;
     __half* os = static_cast<__half*>(o) + (size_t)pl.start * row;
     if (int r = verify_common(shape, layer, seqs, pl.count, nullptr, nullptr, qs, parents, pl.t, path,
-                              ws + kParentsBytes, ws_bytes - kParentsBytes, dev_status, stream))
+                              ws + kParentsBytes, ws_bytes - kParentsBytes, dev_status, stream, nullptr, 0, nullptr,
+                              false))
       return r;
-    return stv_split_combine(shape, seqs, pl.count, pl.t, ws + kParentsBytes, ws_bytes - kParentsBytes, os, stream);
+    return combine_common(shape, seqs, pl.count, pl.t, ws + kParentsBytes, ws_bytes - kParentsBytes, os, stream,
+                          false);
   });
 }
 

@@ -1,6 +1,7 @@
 // prefill_tc.cu -- f2, prefill attention over the 3-bit cache (exact path):
 // a persistent kernel over (chunk, KV head) units, on the 5th-generation
-// tensor cores.
+// tensor cores.  The same kernel, in its verify mode, runs a4 for a batch of
+// several sequences (see "Verify mode" below).
 //
 // Sources: "elpis" README, "Why fast" (prefill over the quantized KV cache:
 // int8 Q.K^T 3021c, a double-buffered K/V ring 3022).  The prompt's own K/V
@@ -27,6 +28,16 @@
 // starts the accumulator afresh.
 // Every wait is bounded; a timeout sets a CTA abort flag, every role stops,
 // in-flight copies and MMAs are waited for (bounded) and TMEM is freed.
+//
+// Verify mode (a2..a4, exact path, a batch of several sequences; Reddit
+// posts (u/iamMess), second post: split-KV verify).  A unit is one work
+// unit of the verify split plan, (sequence, KV head, range of 64-key tiles),
+// and writes its partial O, m, l for split_combine as the verify kernel does.
+// The plan may hold more units than SMs: the host orders them longest first
+// (VerifyParams::order) and the CTAs take them in snake order, so a batch of
+// unequal sequences keeps every SM busy to the end (with one unit per CTA,
+// the longest sequence's units would set the launch's time).  The mask is
+// the sequence's tree mask; the pipeline carries on across units as above.
 #include "stv_device.cuh"
 #include "tc_util.cuh"
 
@@ -72,6 +83,7 @@ __device__ __forceinline__ int unit_of(int k, int b) {
   return k * n + ((k & 1) ? n - 1 - b : b);
 }
 
+// Prefill: unit u is (chunk, KV head), chunks longest (last) first.
 struct Unit {
   int c, h;      // chunk, KV head
   int t, R;      // tokens of the chunk, query rows (t * G)
@@ -92,10 +104,59 @@ __device__ __forceinline__ Unit unit_info(const PrefillParams& p, int u) {
   return x;
 }
 
+// Verify: the w-th longest unit of the split plan (units are numbered
+// sequence-major, then KV head, then split).
+struct VerifyUnit {
+  int h;                       // KV head
+  int slot;                    // the work unit whose partials this writes
+  int s;                       // sequence
+  int node0;                   // Q row of the sequence's first node: [node][hq][256]
+  int R;                       // query rows (T * G)
+  int ctx;                     // keys before the tree
+  int tok0, tok1;              // keys of the unit: [tok0, tok1)
+  int n_tiles;
+  const int32_t* page_table;   // the sequence's pages
+  int n_pages;
+};
+
+__device__ __forceinline__ VerifyUnit unit_info(const VerifyParams& p, int w) {
+  VerifyUnit x;
+  const int u = p.order[w];
+  int s = 0;
+  while (s + 1 < p.n_seqs && u >= p.seq[s + 1].unit_base) ++s;
+  const SeqDesc& sd = p.seq[s];
+  const int local = u - sd.unit_base;
+  x.h = local / sd.splits;
+  x.slot = u;
+  x.s = s;
+  x.node0 = s * p.T;
+  x.R = p.R;
+  x.ctx = sd.ctx;
+  x.tok0 = (local % sd.splits) * p.tiles_per_split * kTileTok;
+  x.tok1 = min(sd.ctx + p.T, x.tok0 + p.tiles_per_split * kTileTok);
+  x.n_tiles = (x.tok1 - x.tok0 + kTileTok - 1) / kTileTok;
+  x.page_table = sd.page_table;
+  x.n_pages = sd.n_pages;
+  return x;
+}
+
+template <bool kVerify>
+struct ParamsOf {
+  using type = PrefillParams;
+  using unit = Unit;
+};
+template <>
+struct ParamsOf<true> {
+  using type = VerifyParams;
+  using unit = VerifyUnit;
+};
+
 // kWithhold (failure-path test only, stv_prefill_attn_timeout_test): the
 // producer issues no copy, so every wait on one runs out.
-template <bool kWithhold>
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ PrefillParams p) {
+// kVerify: verify mode (VerifyParams; exact path, 3-bit cache).
+template <bool kWithhold, bool kVerify>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ typename ParamsOf<kVerify>::type p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment of the operand tiles (the swizzle works on address bits).
   const uint32_t base_u32 = su32(smem_raw);
@@ -154,16 +215,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       for (int k = 0; ok; ++k) {
         const int u = unit_of(k, cta);
         if (u >= p.n_units) break;
-        const Unit x = unit_info(p, u);
+        const auto x = unit_info(p, u);
         for (int i = 0; i < (kWithhold ? 0 : x.n_tiles); ++i) {
           const int st = g % kStages;
           if (!wait1(&bars->raw_empty[st], ((g / kStages) & 1) ^ 1, abort_flag)) {
             ok = false;
             break;
           }
-          const int key0 = i * kTileTok;
-          const int lp = key0 >> 8;
-          int32_t page = lp < p.n_pages ? __ldg(p.page_table + lp) : -1;
+          int key0, lp;
+          int32_t page;
+          if constexpr (kVerify) {
+            key0 = x.tok0 + i * kTileTok;
+            lp = key0 >> 8;
+            page = lp < x.n_pages ? __ldg(x.page_table + lp) : -1;
+          } else {
+            key0 = i * kTileTok;
+            lp = key0 >> 8;
+            page = lp < p.n_pages ? __ldg(p.page_table + lp) : -1;
+          }
           if (page < 0 || page >= p.pool_pages) {
             report(p.status, STV_DEV_BAD_PAGE);
             page = 0;  // read a valid page; the result is flagged as garbage
@@ -213,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     for (int k = 0; ok; ++k) {
       const int u = unit_of(k, cta);
       if (u >= p.n_units) break;
-      const Unit x = unit_info(p, u);
+      const auto x = unit_info(p, u);
       if (!(ok = waitw(&bars->q_ready, k & 1, abort_flag))) break;
       tc_after();
       for (int i = 0; ok && i < 2 && i < x.n_tiles; ++i) ok = issue_qk(g0 + i);
@@ -249,10 +318,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const float c = kLog2e / 16.f;
     // Q rows of a unit -> TMEM columns [0, 128): row r = node * G + (Q head
     // within the KV head); rows past t * G are zero.
-    auto load_q = [&](const Unit& x) {
+    using U = typename ParamsOf<kVerify>::unit;
+    auto load_q = [&](const U& x) {
       const bool live = r < x.R;
       const int node = live ? r / p.G : 0;
-      const int64_t qrow = live ? ((int64_t)(x.c * p.chunk + node) * p.hq + x.h * p.G + r % p.G) : 0;
+      int64_t qrow = 0;
+      if constexpr (kVerify) qrow = live ? ((int64_t)(x.node0 + node) * p.hq + x.h * p.G + r % p.G) : 0;
+      else qrow = live ? ((int64_t)(x.c * p.chunk + node) * p.hq + x.h * p.G + r % p.G) : 0;
 #pragma unroll
       for (int chunk = 0; chunk < 4; ++chunk) {
         uint32_t v[32];
@@ -280,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     bool ok = true;
     int g0 = 0;
     int u = unit_of(0, cta);
-    Unit x = {};
+    U x = {};
     if (u < p.n_units) {
       x = unit_info(p, u);
       load_q(x);
@@ -288,8 +360,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     for (int k = 0; ok && u < p.n_units; ++k) {
       const bool live = r < x.R;
       const int node = live ? r / p.G : 0;
-      // chain tree: node i sees prompt tokens 0..i of its chunk
-      const uint32_t anc = node >= 31 ? 0xffffffffu : ((2u << node) - 1u);
+      uint32_t anc;
+      if constexpr (kVerify) {
+        // a2: this row's ancestor-or-self mask, from the sequence's parent[]
+        anc = 1u << node;
+        const int32_t* par = p.parent + (int64_t)x.s * p.T;
+        for (int n = node, st = 0; st < p.T && n > 0; ++st) {
+          const int pa = __ldg(par + n);
+          if (pa < 0 || pa >= n) {
+            report(p.status, STV_DEV_BAD_TREE);
+            break;
+          }
+          anc |= 1u << pa;
+          n = pa;
+        }
+        if (r == 0 && __ldg(par) != -1) report(p.status, STV_DEV_BAD_TREE);
+      } else {
+        // chain tree: node i sees prompt tokens 0..i of its chunk
+        anc = node >= 31 ? 0xffffffffu : ((2u << node) - 1u);
+      }
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < x.n_tiles; ++j) {
         const int g = g0 + j, b = g & 1;
@@ -300,8 +389,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         tmem_ld32(lane_addr + kColS0 + 64 * b + 32, sb);
         tmem_wait_ld(sa);
         tmem_wait_ld(sb);
-        const int key0 = j * kTileTok;
-        if (key0 + kTileTok > x.ctx) {
+        int key0;
+        bool edge;
+        if constexpr (kVerify) {
+          key0 = x.tok0 + j * kTileTok;
+          edge = key0 + kTileTok > x.ctx || key0 + kTileTok > x.tok1;
+        } else {
+          key0 = j * kTileTok;
+          edge = key0 + kTileTok > x.ctx;
+        }
+        if (edge) {
           // Visibility of the tile's 64 keys as one bit mask: keys before the
           // chunk, this row's own and earlier chunk tokens, nothing at or past
           // the chunk's end.  Masked keys become -inf by selection.
@@ -382,29 +479,51 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       if (!ok) break;
       // The next unit's Q: every Q.K^T of this unit has completed.
       const int un = unit_of(k + 1, cta);
-      Unit xn = {};
+      U xn = {};
       if (un < p.n_units) {
         xn = unit_info(p, un);
         load_q(xn);
       }
-      // ---- epilogue: O / l of this row, fp16, into the output ----
       if (!(ok = waitw(&bars->o_ready, k & 1, abort_flag))) break;
       tc_after();
-      __half* dst = p.o + ((int64_t)(x.c * p.chunk + node) * p.hq + x.h * p.G + r % p.G) * kHeadDim;
+      if constexpr (kVerify) {
+        // ---- epilogue: O, m, l of this row into the unit's partials ----
+        float* dst = p.o_part + ((int64_t)x.slot * x.R + r) * kHeadDim;
 #pragma unroll 1
-      for (int chunk = 0; chunk < 8; ++chunk) {
-        uint32_t o[32];
-        tmem_ld32(lane_addr + kColO + 32 * chunk, o);
-        tmem_wait_ld(o);
-        if (live) {  // l >= 1 for a live row: its own key is visible and P(max) >= 2^-8
+        for (int chunk = 0; chunk < 8; ++chunk) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + kColO + 32 * chunk, o);
+          tmem_wait_ld(o);
+          if (live) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 w;
-            w.x = h2u(__floats2half2_rn(__uint_as_float(o[8 * e]) / l, __uint_as_float(o[8 * e + 1]) / l));
-            w.y = h2u(__floats2half2_rn(__uint_as_float(o[8 * e + 2]) / l, __uint_as_float(o[8 * e + 3]) / l));
-            w.z = h2u(__floats2half2_rn(__uint_as_float(o[8 * e + 4]) / l, __uint_as_float(o[8 * e + 5]) / l));
-            w.w = h2u(__floats2half2_rn(__uint_as_float(o[8 * e + 6]) / l, __uint_as_float(o[8 * e + 7]) / l));
-            reinterpret_cast<uint4*>(dst + 32 * chunk)[e] = w;
+            for (int e = 0; e < 8; ++e)
+              reinterpret_cast<float4*>(dst + 32 * chunk)[e] =
+                  make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                              __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+          }
+        }
+        if (live) {
+          p.ml[((int64_t)x.slot * x.R + r) * 2] = m_ref;
+          p.ml[((int64_t)x.slot * x.R + r) * 2 + 1] = l;
+        }
+      } else {
+        // ---- epilogue: O / l of this row, fp16, into the output ----
+        __half* dst = p.o + ((int64_t)(x.c * p.chunk + node) * p.hq + x.h * p.G + r % p.G) * kHeadDim;
+#pragma unroll 1
+        for (int chunk = 0; chunk < 8; ++chunk) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + kColO + 32 * chunk, o);
+          tmem_wait_ld(o);
+          if (live) {  // l >= 1 for a live row: its own key is visible and P(max) >= 2^-8
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              uint4 w;
+              w.x = h2u(__floats2half2_rn(__uint_as_float(o[8 * e]) / l, __uint_as_float(o[8 * e + 1]) / l));
+              w.y = h2u(__floats2half2_rn(__uint_as_float(o[8 * e + 2]) / l, __uint_as_float(o[8 * e + 3]) / l));
+              w.z = h2u(__floats2half2_rn(__uint_as_float(o[8 * e + 4]) / l, __uint_as_float(o[8 * e + 5]) / l));
+              w.w = h2u(__floats2half2_rn(__uint_as_float(o[8 * e + 6]) / l, __uint_as_float(o[8 * e + 7]) / l));
+              reinterpret_cast<uint4*>(dst + 32 * chunk)[e] = w;
+            }
           }
         }
       }
@@ -429,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     for (int k = 0; ok; ++k) {
       const int u = unit_of(k, cta);
       if (u >= p.n_units) break;
-      const Unit x = unit_info(p, u);
+      const auto x = unit_info(p, u);
       for (int i = 0; i < x.n_tiles; ++i) {
         const int st = g % kStages, b = g & 1, vb = g % kVBuffers;
         const uint8_t* stage = ring + st * kStageBytes;
@@ -467,7 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           // this channel's group: 64 key scales, as 32 (key 2m, 2m+1) pairs
           const uint4* sp = reinterpret_cast<const uint4*>(stage + kKTileCodeBytes + kKTileScaleBytes +
                                                            kVTileCodeBytes + (vch >> 5) * (kTileTok * 2));
-          const int live = x.tok1 - i * kTileTok;  // keys at or beyond this are zeroed
+          int live;  // keys at or beyond this are zeroed
+          if constexpr (kVerify) live = x.tok1 - (x.tok0 + i * kTileTok);
+          else live = x.tok1 - i * kTileTok;
           const uint32_t vrow = su32(vdeq0) + vb * kOperandBytes + sw128_row(vch);
 #pragma unroll
           for (int blk = 0; blk < 2; ++blk) {
@@ -515,10 +636,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillParams& p, int grid, cudaStream_t s, bool withhold_copies) {
-  auto kernel = withhold_copies ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+  auto kernel = withhold_copies ? prefill_tc_kernel<true, false> : prefill_tc_kernel<false, false>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   return launch_pdl(kernel, grid, kThreads, kSmemBytes, s, p);
+}
+
+cudaError_t launch_verify_persistent(const VerifyParams& p, cudaStream_t s) {
+  auto kernel = prefill_tc_kernel<false, true>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kernel, p.persist_ctas, kThreads, kSmemBytes, s, p);
 }
 
 }  // namespace stv

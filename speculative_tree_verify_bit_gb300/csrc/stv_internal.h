@@ -19,6 +19,10 @@ constexpr int kTileTok = 64;                 // V-code tiles and verify tiles
 constexpr int kMaxRows = 128;                // T * G per KV head
 constexpr int kMaxT = 32;
 constexpr int kMaxSplitsPerHead = 256;  // split_combine keeps one (m, l) per split in 8 registers x 32 lanes
+// A balanced plan (several sequences, 3-bit cache) may hold up to this many
+// work units; the persistent verify kernel takes them in the order
+// VerifyParams::order gives.
+constexpr int kMaxPersistUnits = 640;
 
 // Byte offsets inside one KV head's block of a page (see include/stv.h).
 constexpr int kOffKCodes = 0;
@@ -74,6 +78,11 @@ struct Plan {
   int tiles_per_split;
   int splits[STV_MAX_SEQS];
   int unit_base[STV_MAX_SEQS + 1];
+  // Balanced plan (make_plan with balance, several sequences, 3-bit cache):
+  // the persistent verify kernel's CTAs (0 otherwise) and the units, longest
+  // first.
+  int persist_ctas;
+  int16_t order[kMaxPersistUnits];
 };
 
 // Workspace carve-up (byte offsets, each 256-aligned).
@@ -130,6 +139,12 @@ struct VerifyParams {
   uint32_t* cnt;
   int n_pairs;
   int packed_target;  // packing warps that arrive: min(n_units, n_pairs)
+  // Balanced plan: the exact path on the 3-bit cache runs the persistent
+  // kernel (prefill_tc.cu, verify mode) on persist_ctas CTAs, which take the
+  // units order[0], order[1], ... (longest first) in snake order; 0 = one
+  // CTA per unit.
+  int persist_ctas;
+  int16_t order[kMaxPersistUnits];
 };
 
 // Parameters of one prefill launch (prefill_tc.cu, exact path, 3-bit cache):
@@ -234,7 +249,7 @@ cudaError_t launch_pdl_coop(void (*kernel)(KArgs...), int grid, int block, size_
 }
 
 // ---- host helpers (api.cu) ----
-int make_plan(const ShapeInfo& sh, const stv_seq* seqs, int n_seqs, int sm_count, Plan* plan);
+int make_plan(const ShapeInfo& sh, const stv_seq* seqs, int n_seqs, int sm_count, Plan* plan, bool balance);
 WsLayout ws_layout(const ShapeInfo& sh, int n_seqs, const Plan& plan);
 
 // ---- launchers (return cudaError_t of the launch) ----
@@ -247,6 +262,7 @@ cudaError_t launch_verify_i8(const VerifyParams& p, cudaStream_t s);  // int8 pa
 cudaError_t launch_split_combine(const CombineParams& p, cudaStream_t s);
 // prefill_tc.cu; withhold_copies: failure-path test (every wait runs out)
 cudaError_t launch_prefill(const PrefillParams& p, int grid, cudaStream_t s, bool withhold_copies = false);
+cudaError_t launch_verify_persistent(const VerifyParams& p, cudaStream_t s);  // prefill_tc.cu, verify mode
 cudaError_t launch_tree_accept(const int32_t* parent, const int32_t* draft, const int32_t* argmax, int T, int n_seqs,
                                int32_t* n_commit, int32_t* path, int32_t* out_ids, int32_t* status, cudaStream_t s);
 

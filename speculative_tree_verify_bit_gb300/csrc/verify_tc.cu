@@ -904,6 +904,8 @@ cudaError_t launch_one(const VerifyParams& p, cudaStream_t s) {
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s) {
   // the int8 path on the 3-bit cache forms per-group integer dots: its own kernel
   if (p.path == STV_PATH_INT8 && p.fmt == kFmtBit3) return launch_verify_i8(p, s);
+  // a balanced plan for several sequences: the persistent kernel (exact path, 3-bit cache)
+  if (p.persist_ctas > 0) return launch_verify_persistent(p, s);
   // one launch per layer: append, verify and merge (exact path, 3-bit cache)
   if (p.o_out)
     return p.tiles_per_split <= kStagedEpilogueTiles ? launch_one<false, kFmtBit3, false, true, true>(p, s)

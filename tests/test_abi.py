@@ -85,6 +85,72 @@ def test_workspace_units_never_exceed_sm_count(lib):
         assert rc1 == 0 and rc2 == 0 and big >= small
 
 
+def _balanced_units(ctxs, t, hkv, sm, rows):
+    """The split plan for several sequences on the 3-bit cache, restated: the
+    one-unit-per-SM split k0, then the split k in [k0 / 4, k0) whose units,
+    dealt longest first in snake order to min(SMs, units) CTAs at (tiles + 3)
+    each, finish first (ties to the larger k), within 640 units and 24 MiB of
+    partials."""
+    tiles = [-(-(c + t) // 64) for c in ctxs]
+    total = hkv * sum(tiles)
+    k_min = max([1] + [-(-x // 256) for x in tiles])
+    k0 = max(-(-total // sm), k_min)
+    while sum(hkv * -(-x // k0) for x in tiles) > max(sm, len(tiles) * hkv):
+        k0 += 1
+
+    def lengths(k):
+        return [min(k, x - j * k) for x in tiles for _ in range(hkv) for j in range(-(-x // k))]
+
+    def makespan(lens):
+        n = min(sm, len(lens))
+        load = [0] * n
+        for w, ln in enumerate(sorted(lens, reverse=True)):
+            kk, b = divmod(w, n)
+            load[n - 1 - b if kk % 2 else b] += ln + 3
+        return max(load)
+
+    best_k, best = k0, makespan(lengths(k0))
+    for k in range(k0 - 1, max(k_min, k0 // 4) - 1, -1):
+        lens = lengths(k)
+        if len(lens) > 640 or len(lens) * rows * 1024 > 24 << 20:
+            break
+        c = makespan(lens)
+        if c < best:
+            best_k, best = k, c
+    return sum(hkv * -(-x // best_k) for x in tiles)
+
+
+@pytest.mark.parametrize("ctxs", [[1024 << i for i in range(8)], [300, 0, 1000, 2047], [131072, 131072],
+                                  [100000, 20000, 5000], [40000] + [500] * 20])
+def test_balanced_plan_for_several_sequences(lib, ctxs):
+    """Several sequences on the 3-bit cache: the plan may hold more units
+    than SMs (the persistent verify kernel deals them longest first); the
+    workspace holds that plan's partials."""
+    units = _balanced_units(ctxs, 16, 4, 152, 96)
+    pages = [-(-(c + 16) // 256) for c in ctxs]
+    rc, nbytes = _ws(stv.make_shape(), ctxs, pages, 16, 152)
+    assert rc == 0
+    n = len(ctxs)
+    a = lambda x: (x + 255) // 256 * 256
+    cnt = (2 + 64 * 4) * 4
+    assert nbytes == a(a(a(a(cnt) + n * 16 * 24 * 256) + n * 16 * 24 * 4) + units * 96 * 256 * 4) + units * 96 * 2 * 4
+    if ctxs[0] == 1024:
+        assert units == 168  # 109 tiles per split: 152 long units and 16 short ones
+
+
+def test_balanced_plan_is_for_the_three_bit_cache_only(lib):
+    """The int4 cache keeps one unit per SM (its kernel is not persistent)."""
+    ctxs = [1024 << i for i in range(8)]
+    pages = [-(-(c + 16) // 256) for c in ctxs]
+    rc, nbytes = _ws(stv.make_shape(group=256), ctxs, pages, 16, 152)
+    assert rc == 0
+    a = lambda x: (x + 255) // 256 * 256
+    units = 4 * sum(-(-(-(-(c + 16) // 64)) // 129) for c in ctxs)  # 129 tiles per split
+    assert units == 136
+    cnt = (2 + 64 * 4) * 4
+    assert nbytes == a(a(a(a(cnt) + 8 * 16 * 24 * 256) + 8 * 16 * 24 * 4) + units * 96 * 256 * 4) + units * 96 * 2 * 4
+
+
 def test_split_plan_caps_splits_per_head(lib):
     # 2^20 + 16 keys = 16,385 tiles per KV head.  Planned for 10,000 SMs the
     # plan would cut them finer than the 256 splits split_combine accepts, so

@@ -171,6 +171,30 @@ def test_bad_tree_flagged(gpu):
     assert int(status.item()) & stv.STV_DEV_BAD_TREE
 
 
+def test_bad_tree_flagged_batch(gpu):
+    """The same check in a batch of several sequences (the persistent kernel)."""
+    r = Round([3000, 100], 4, seed=8, parents=[[-1, 0, 1, 2], [-1, 0, 5, 1]])
+    r.gpu_cache()
+    ws = torch.empty(stv.stv_verify_workspace_bytes(r.shape, r.seqs, 4), dtype=torch.uint8, device=gpu)
+    status = torch.zeros(1, dtype=torch.int32, device=gpu)
+    stv.stv_verify_attn(r.shape, r.layer, r.seqs, r.q, torch.as_tensor(r.parent, device=gpu), 4, "exact", ws,
+                        dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & stv.STV_DEV_BAD_TREE
+
+
+def test_ragged_full_size_deterministic(gpu):
+    """Eight requests, 1K..128K: the balanced plan (more units than SMs, the
+    persistent kernel dealing them longest first) gives the same bytes on
+    every run."""
+    w = workloads.WORKLOADS["ragged"]
+    r = Round(list(w.ctx), w.t_nodes, seed=workloads.layer_seed(w, 3))
+    r.gpu_cache()
+    a = r.gpu_verify("exact")
+    b = r.gpu_verify("exact")
+    assert torch.equal(a, b)
+
+
 def test_workspace_too_small_rejected(gpu):
     r = Round([100], 4, seed=7)
     r.gpu_cache()
