@@ -59,9 +59,6 @@ constexpr int kSmemBytes = 1024 /*align slack*/ + (2 + kVBuffers) * kOperandByte
 // issues only after the softmax of tile i has arrived on p_full, so a slot is
 // never rewritten while it is read.
 constexpr int kKScaleSlots = 4;
-// Work units of at most this many tiles take the staged epilogue (measured at
-// T = 16: 14-tile units gain about 1 us per launch, 108-tile units lose 2 us).
-constexpr int kStagedEpilogueTiles = 48;
 template <int kFmt>
 struct Fmt {  // the 3-bit cache
   static constexpr int stages = kStages;
@@ -133,8 +130,9 @@ __device__ __forceinline__ bool settle(uint64_t* b, uint32_t parity, uint32_t pr
 // TMEM -> shared memory, its 16-byte pieces XOR-swizzled by row mod 8 so the
 // warp's stores spread over the banks; then the warp copies the rows out one
 // at a time, a lane per 16 bytes: coalesced 512-byte stores instead of 32
-// lanes writing 32 rows 1 KiB apart.  Out of line, so the tile loop's code
-// does not change with it.
+// lanes writing 32 rows 1 KiB apart (measured: 262K 119.6 -> 117.2 us per
+// layer-round, 32K unchanged).  Out of line, so the tile loop's code does
+// not change with it.
 __device__ __noinline__ void epilogue_rows_staged(uint32_t lane_addr, uint8_t* stage, float* dst0, int quad, int R) {
   const int lane = threadIdx.x & 31, r = quad * 32 + lane;
   const uint32_t srow = su32(stage) + (uint32_t)r * 1024u;
@@ -245,16 +243,12 @@ __device__ __noinline__ void fused_merge(const VerifyParams& p, volatile int* ab
 // (stv_append_verify_attn); the plain instantiation carries none of that code.
 // kWithhold (failure-path test only, stv_verify_attn_timeout_test): the
 // producer issues no copy, so every wait on one runs out.
-// kStaged: the epilogue stages O through shared memory (launches whose work
-// units are short, where the epilogue is a large part of the launch; on long
-// units the out-of-line call's registers slow the tile loop more than the
-// coalesced stores save).
 // kFused: one launch per layer (stv_append_verify_combine, cooperative): a
 // fifteenth warp packs the round's tree rows (fused_pack_tree_rows), a unit
 // copies a tile holding tree keys once every packing warp of the launch has
 // arrived on a device counter, and after the teardown the units merge the
 // splits (fused_merge).
-template <bool kAppend, int kFmt, bool kWithhold = false, bool kStaged = false, bool kFused = false>
+template <bool kAppend, int kFmt, bool kWithhold = false, bool kFused = false>
 __global__ void __launch_bounds__(kFused ? kThreads + 32 : kThreads, 1)
     verify_tc_kernel(const __grid_constant__ VerifyParams p) {
   using F = Fmt<kFmt>;
@@ -603,24 +597,7 @@ __global__ void __launch_bounds__(kFused ? kThreads + 32 : kThreads, 1)
     if (ok) ok = waitw(&bars->mma_done, 0, abort_flag);
     if (ok) {
       tc_after();
-      if constexpr (kStaged) {
-        epilogue_rows_staged(lane_addr, kdeq0, p.o_part + (int64_t)blockIdx.x * R * kHeadDim, quad, R);
-      } else {
-        float* dst = p.o_part + ((int64_t)blockIdx.x * R + r) * kHeadDim;
-#pragma unroll 1
-        for (int chunk = 0; chunk < 8; ++chunk) {
-          uint32_t o[32];
-          tmem_ld32(lane_addr + kColO + 32 * chunk, o);
-          tmem_wait_ld(o);
-          if (r < R) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              reinterpret_cast<float4*>(dst + 32 * chunk)[e] =
-                  make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
-                              __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
-          }
-        }
-      }
+      epilogue_rows_staged(lane_addr, kdeq0, p.o_part + (int64_t)blockIdx.x * R * kHeadDim, quad, R);
       if (r < R) {
         p.ml[((int64_t)blockIdx.x * R + r) * 2] = m_ref;
         p.ml[((int64_t)blockIdx.x * R + r) * 2 + 1] = l;
@@ -894,9 +871,9 @@ __global__ void __launch_bounds__(kFused ? kThreads + 32 : kThreads, 1)
   if (tid == 0 && bars->abort) report(p.status, STV_DEV_TIMEOUT);
 }
 
-template <bool kAppend, int kFmt, bool kWithhold = false, bool kStaged = false, bool kFused = false>
+template <bool kAppend, int kFmt, bool kWithhold = false, bool kFused = false>
 cudaError_t launch_one(const VerifyParams& p, cudaStream_t s) {
-  auto kernel = verify_tc_kernel<kAppend, kFmt, kWithhold, kStaged, kFused>;
+  auto kernel = verify_tc_kernel<kAppend, kFmt, kWithhold, kFused>;
   constexpr int smem = Fmt<kFmt>::smem;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -912,9 +889,7 @@ cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s) {
   // a balanced plan for several sequences: the persistent kernel (exact path, 3-bit cache)
   if (p.persist_ctas > 0) return launch_verify_persistent(p, s);
   // one launch per layer: append, verify and merge (exact path, 3-bit cache)
-  if (p.o_out)
-    return p.tiles_per_split <= kStagedEpilogueTiles ? launch_one<false, kFmtBit3, false, true, true>(p, s)
-                                                      : launch_one<false, kFmtBit3, false, false, true>(p, s);
+  if (p.o_out) return launch_one<false, kFmtBit3, false, true>(p, s);
   if (p.test_withhold_copies)
     return p.fmt == kFmtInt4 ? launch_one<false, kFmtInt4, true>(p, s) : launch_one<false, kFmtBit3, true>(p, s);
   // the fused append packs the 3-bit cache only (the host refuses it for the others)
@@ -922,8 +897,7 @@ cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s) {
   if (p.fmt == kFmtInt4) return launch_one<false, kFmtInt4>(p, s);
   if (p.fmt == kFmtK4V2) return launch_one<false, kFmtK4V2>(p, s);
   if (append) return launch_one<true, kFmtBit3>(p, s);
-  return p.tiles_per_split <= kStagedEpilogueTiles ? launch_one<false, kFmtBit3, false, true>(p, s)
-                                                    : launch_one<false, kFmtBit3>(p, s);
+  return launch_one<false, kFmtBit3>(p, s);
 }
 
 }  // namespace stv
