@@ -234,6 +234,13 @@ int stv_verify_attn(const stv_shape* shape, const stv_layer_cache* layer, const 
  *  k_tree, v_tree: device fp16 [n_seqs][T][hkv][256], caller-owned, read only.
  *  All other arguments, the workspace and the results as in stv_verify_attn;
  *  the cache bytes written equal those of stv_kv_append_pack on the same rows.
+ *  Exact path, one work unit per SM (one sequence): the rows are packed by an
+ *  extra warp of every unit, the pairs (row, KV head) dealt round-robin, and
+ *  a unit copies a tile holding tree keys once every pair is packed (a
+ *  cooperative launch; the workspace's arrival counters, as for
+ *  stv_append_verify_combine, must be zero before the first call and every
+ *  completed call leaves them zero).  Otherwise (the int8 path, several
+ *  sequences) the unit whose key range holds a tree row packs it.
  *  STV_ERR_INVALID_ARG when k_tree or v_tree is null; a page-table entry
  *  outside the pool sets STV_DEV_BAD_PAGE and that row is not written.
  */

@@ -266,7 +266,9 @@ def stv_append_verify_attn(shape, layer: LayerCache, seqs, k_tree, v_tree, q, pa
                            dev_status=None, stream=None):
     """stv_kv_append_pack of the round's tree rows (k_tree, v_tree: fp16
     [n_seqs][T][hkv][256], row i of sequence s at ctx_s + i) fused into
-    stv_verify_attn: one launch."""
+    stv_verify_attn: one launch.  The workspace must be zero-filled before
+    its first use here (arrival counters of the exact path's packing warp);
+    each completed call leaves them zero."""
     import torch
 
     lc = layer.c()

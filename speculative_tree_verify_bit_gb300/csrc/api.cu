@@ -407,8 +407,15 @@ static int verify_common(const stv_shape* shape, const stv_layer_cache* layer, c
     p.persist_ctas = plan.persist_ctas;
     memcpy(p.order, plan.order, sizeof(int16_t) * plan.n_units);
   }
-  if (o_fused) {
+  // The fused append's packing warp (tree rows packed by all units, the
+  // tile's copy waiting on a device counter) needs every unit resident at
+  // once: the exact path on the 3-bit cache with one unit per SM; otherwise
+  // (the int8 path, a balanced plan) the units holding tree rows pack them.
+  const bool pack_warp = k_tree && !o_fused && path == STV_PATH_EXACT && sh.fmt == kFmtBit3 &&
+                         plan.persist_ctas == 0 && plan.n_units <= sm && !withhold_copies;
+  if (o_fused || pack_warp) {
     p.o_out = static_cast<__half*>(o_fused);
+    p.pack_warp = pack_warp ? 1 : 0;
     p.cnt = reinterpret_cast<uint32_t*>(ws + wl.off_cnt);
     p.n_pairs = n_seqs * sh.T * sh.hkv;
     p.packed_target = std::min(p.n_units, p.n_pairs);  // one packing warp per unit that has a pair

@@ -139,6 +139,9 @@ struct VerifyParams {
   uint32_t* cnt;
   int n_pairs;
   int packed_target;  // packing warps that arrive: min(n_units, n_pairs)
+  // The fused append by the packing warp without the merge (o_out null):
+  // stv_append_verify_attn when the plan keeps one unit per SM.
+  int pack_warp;
   // Balanced plan: the exact path on the 3-bit cache runs the persistent
   // kernel (prefill_tc.cu, verify mode) on persist_ctas CTAs, which take the
   // units order[0], order[1], ... (longest first) in snake order; 0 = one

@@ -206,11 +206,14 @@ __device__ __noinline__ void fused_pack_tree_rows(const VerifyParams& p) {
 // next launch: every unit has passed every wait of this one by then.
 __device__ __noinline__ void fused_merge(const VerifyParams& p, volatile int* abort_flag, int my_s, int my_h) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, n_warps = blockDim.x >> 5;
-  if (tid == 0) {
+  // the fused append alone (stv_append_verify_attn): no merge, only the
+  // counters' reset below
+  const bool merge = p.o_out != nullptr;
+  if (merge && tid == 0) {
     __threadfence();
     atomicAdd(p.cnt + 2 + my_s * p.hkv + my_h, 1u);
   }
-  const int per_head = 4 * p.R, n_items = p.n_seqs * p.hkv * per_head;
+  const int per_head = 4 * p.R, n_items = merge ? p.n_seqs * p.hkv * per_head : 0;
   const int i0 = (int)((int64_t)blockIdx.x * n_items / p.n_units);
   const int i1 = (int)((int64_t)(blockIdx.x + 1) * n_items / p.n_units);
   int waited = -1;
@@ -243,11 +246,12 @@ __device__ __noinline__ void fused_merge(const VerifyParams& p, volatile int* ab
 // (stv_append_verify_attn); the plain instantiation carries none of that code.
 // kWithhold (failure-path test only, stv_verify_attn_timeout_test): the
 // producer issues no copy, so every wait on one runs out.
-// kFused: one launch per layer (stv_append_verify_combine, cooperative): a
-// fifteenth warp packs the round's tree rows (fused_pack_tree_rows), a unit
-// copies a tile holding tree keys once every packing warp of the launch has
-// arrived on a device counter, and after the teardown the units merge the
-// splits (fused_merge).
+// kFused (cooperative launch): a fifteenth warp packs the round's tree rows
+// (fused_pack_tree_rows), a unit copies a tile holding tree keys once every
+// packing warp of the launch has arrived on a device counter, and after the
+// teardown the units merge the splits (fused_merge) -- one launch per layer,
+// stv_append_verify_combine -- or, with no output given, leave the partials
+// to split_combine (stv_append_verify_attn for one sequence).
 template <bool kAppend, int kFmt, bool kWithhold = false, bool kFused = false>
 __global__ void __launch_bounds__(kFused ? kThreads + 32 : kThreads, 1)
     verify_tc_kernel(const __grid_constant__ VerifyParams p) {
@@ -888,8 +892,9 @@ cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s) {
   if (p.path == STV_PATH_INT8 && p.fmt == kFmtBit3) return launch_verify_i8(p, s);
   // a balanced plan for several sequences: the persistent kernel (exact path, 3-bit cache)
   if (p.persist_ctas > 0) return launch_verify_persistent(p, s);
-  // one launch per layer: append, verify and merge (exact path, 3-bit cache)
-  if (p.o_out) return launch_one<false, kFmtBit3, false, true>(p, s);
+  // the packing warp: one launch per layer (append, verify, merge), or the
+  // fused append alone (exact path, 3-bit cache)
+  if (p.o_out || p.pack_warp) return launch_one<false, kFmtBit3, false, true>(p, s);
   if (p.test_withhold_copies)
     return p.fmt == kFmtInt4 ? launch_one<false, kFmtInt4, true>(p, s) : launch_one<false, kFmtBit3, true>(p, s);
   // the fused append packs the 3-bit cache only (the host refuses it for the others)

@@ -41,7 +41,7 @@ def tree_rows(r: Round):
 
 def fused_verify(r: Round, layer, path):
     kt, vt = tree_rows(r)
-    ws = torch.empty(stv.stv_verify_workspace_bytes(r.shape, r.seqs, r.T), dtype=torch.uint8, device=r.device)
+    ws = torch.zeros(stv.stv_verify_workspace_bytes(r.shape, r.seqs, r.T), dtype=torch.uint8, device=r.device)
     o = torch.empty((r.n_seqs, r.T, r.hq, 256), dtype=torch.float16, device=r.device)
     status = torch.zeros(1, dtype=torch.int32, device=r.device)
     stv.stv_append_verify_attn(r.shape, layer, r.seqs, kt, vt, r.q, torch.as_tensor(r.parent, device=r.device), r.T,
@@ -100,7 +100,7 @@ def test_fused_append_full_size_long_context(gpu):
 def test_fused_append_rejects_missing_rows(gpu):
     r = Round([100], 4, seed=71)
     layer = context_only_cache(r)
-    ws = torch.empty(stv.stv_verify_workspace_bytes(r.shape, r.seqs, 4), dtype=torch.uint8, device=gpu)
+    ws = torch.zeros(stv.stv_verify_workspace_bytes(r.shape, r.seqs, 4), dtype=torch.uint8, device=gpu)
     kt, _ = tree_rows(r)
     with pytest.raises(stv.StvError) as e:
         stv.stv_append_verify_attn(r.shape, layer, r.seqs, kt, None, r.q, torch.as_tensor(r.parent, device=gpu), 4,
