@@ -18,6 +18,10 @@
 //   warps 2-5   softmax: thread = query row = TMEM lane (128 rows, the
 //               T*G rows sharing the KV head, zero-padded).
 //   warps 6-13  unpack: 3-bit codes -> fp16 operands in shared memory.
+//   warp 14     (the kFused instantiation only) packs the round's tree rows.
+// The warp index is read from lane 0, so the compiler knows the role
+// branches are warp-uniform.  At the end each softmax warp stages its O rows
+// through the freed operand buffers and writes them coalesced.
 // Tensor memory (512 columns): Q [0,128) as the A operand of S = Q K^T;
 // S0/S1 [128,192) [192,256), double-buffered, where P (fp16) overwrites S as
 // the A operand of O += P V; O [256,512) fp32 accumulators.
