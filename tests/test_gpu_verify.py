@@ -183,6 +183,24 @@ def test_bad_tree_flagged_batch(gpu):
     assert int(status.item()) & stv.STV_DEV_BAD_TREE
 
 
+@pytest.mark.parametrize("path", ["exact", "int8"])
+def test_sixty_four_sequences(gpu, path):
+    """The largest batch: 64 sequences of 0..3,000 cached tokens.  Every
+    (sequence, KV head) takes at least one work unit, so the plan holds more
+    units than SMs: the exact path's persistent kernel takes two or more per
+    CTA, the int8 kernel runs them as waves.  Whole heads of every eighth
+    sequence against the oracle."""
+    rng = np.random.default_rng(64)
+    ctx = [int(c) for c in rng.integers(0, 3000, 64)]
+    r = Round(ctx, 16, seed=6464)
+    r.gpu_cache()
+    r.oracle_cache()
+    got = r.gpu_verify(path).float().cpu().numpy()
+    seqs, heads = range(0, 64, 8), (0, 23)
+    want = r.oracle_attention(path, rows=head_rows(seqs, heads, 16)).reshape(-1, 16, 256)
+    assert_attention_close(gather_heads(got, seqs, heads, 16), want, f"64 sequences/{path}")
+
+
 def test_ragged_full_size_deterministic(gpu):
     """Eight requests, 1K..128K: the balanced plan (more units than SMs, the
     persistent kernel dealing them longest first) gives the same bytes on
