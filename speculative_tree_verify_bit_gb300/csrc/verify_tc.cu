@@ -555,19 +555,23 @@ __global__ void __launch_bounds__(kFused ? kThreads + 32 : kThreads, 1)
         l *= corr;
       }
       // P = 2^(S c - m_ref) in fp16, packed key pairs, into the S columns.
+      // The exponent arguments and the row sum use the paired fp32 FMA and
+      // add (two lanes per instruction, each rounded as its scalar form):
+      // the softmax warps share their issue slots with the unpack warps.
       const float mref = m_ref == -INFINITY ? 0.f : m_ref;
-      float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      const float2 c2 = make_float2(c, c), nm2 = make_float2(-mref, -mref);
+      float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        const float p0 = ex2(fmaf(__uint_as_float(sa[2 * e]), c, -mref));
-        const float p1 = ex2(fmaf(__uint_as_float(sa[2 * e + 1]), c, -mref));
-        const float p2 = ex2(fmaf(__uint_as_float(sb[2 * e]), c, -mref));
-        const float p3 = ex2(fmaf(__uint_as_float(sb[2 * e + 1]), c, -mref));
-        sum8[e & 7] += (p0 + p1) + (p2 + p3);
-        sa[e] = h2u(__floats2half2_rn(p0, p1));
-        sb[e] = h2u(__floats2half2_rn(p2, p3));
+        const float2 xa = __ffma2_rn(make_float2(__uint_as_float(sa[2 * e]), __uint_as_float(sa[2 * e + 1])), c2, nm2);
+        const float2 xb = __ffma2_rn(make_float2(__uint_as_float(sb[2 * e]), __uint_as_float(sb[2 * e + 1])), c2, nm2);
+        const float2 pa = make_float2(ex2(xa.x), ex2(xa.y)), pb = make_float2(ex2(xb.x), ex2(xb.y));
+        sum4[e & 3] = __fadd2_rn(sum4[e & 3], __fadd2_rn(pa, pb));
+        sa[e] = h2u(__floats2half2_rn(pa.x, pa.y));
+        sb[e] = h2u(__floats2half2_rn(pb.x, pb.y));
       }
-      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+      const float2 sum2 = __fadd2_rn(__fadd2_rn(sum4[0], sum4[1]), __fadd2_rn(sum4[2], sum4[3]));
+      l += sum2.x + sum2.y;
       uint32_t pk[32];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
@@ -588,8 +592,13 @@ __global__ void __launch_bounds__(kFused ? kThreads + 32 : kThreads, 1)
             uint32_t o[32];
             tmem_ld32(lane_addr + kColO + 32 * chunk, o);
             tmem_wait_ld(o);
+            const float2 corr2 = make_float2(corr, corr);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+            for (int e = 0; e < 16; ++e) {
+              const float2 x = __fmul2_rn(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), corr2);
+              o[2 * e] = __float_as_uint(x.x);
+              o[2 * e + 1] = __float_as_uint(x.y);
+            }
             tmem_st32(lane_addr + kColO + 32 * chunk, o);
           }
         }
