@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(kFused ? kThreads + 32 : kThreads, 1)
   using F = Fmt<kFmt>;
   constexpr bool kI4 = kFmt == kFmtInt4;    // one K scale per key, handed to the softmax
   constexpr bool kKv2 = kFmt == kFmtK4V2;  // 4-bit K, 2-bit V, scales per 32-channel group
+  constexpr bool kBit3 = !kI4 && !kKv2;    // the 3-bit cache
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment of the operand tiles (the swizzle works on address bits).
   const uint32_t base_u32 = su32(smem_raw);
@@ -623,16 +624,22 @@ __global__ void __launch_bounds__(kFused ? kThreads + 32 : kThreads, 1)
   } else if (warp < 14) {
     // =================== unpack (256 threads) ===================
     const int ut = tid - 6 * 32;
-    // K: key and 64-channel column block.  Each group of 8 consecutive lanes
-    // takes 8 different keys of one column block, so the 8 lanes of a
-    // 128-bit store phase land on 8 different swizzled 16-byte positions.
+    // K: key and 64-channel column block; a warp holds 8 keys x 4 blocks.
+    // The 8 lanes of a 128-bit store phase must land on 8 different
+    // swizzled 16-byte positions (8 different keys of one block, or 4 keys
+    // of two blocks writing opposite halves of their rows).
     // int4: a key's codes are one 128-byte row, so block kcb of every key
     // sits in the same banks; a 128-bit load is served 8 lanes at a time,
     // so the 8 lanes of each group take different blocks (kcb = j/2 + group,
     // mod 4) and start at different halves (j mod 2), which makes the loads
     // conflict-free while the stores keep 8 different keys per group.
-    const int kj = (ut >> 5) * 8 + (ut & 7);
-    const int kcb = (kI4 || kKv2) ? (((ut & 7) >> 1) + ((ut >> 3) & 3)) & 3 : (ut >> 3) & 3;
+    // 3-bit: a key's codes are 96 bytes and a block's 24, so keys four apart
+    // share banks; each half-warp takes 4 keys x 4 blocks (its 64-bit loads
+    // then cover all 32 banks once), and the lanes of an odd block store the
+    // second half of their row first, so that each quarter-warp's (4 keys x
+    // 2 blocks) 128-bit stores still land on 8 different swizzled positions.
+    const int kj = kBit3 ? (ut >> 5) * 8 + (ut & 3) + 4 * ((ut >> 4) & 1) : (ut >> 5) * 8 + (ut & 7);
+    const int kcb = kBit3 ? (ut >> 2) & 3 : (((ut & 7) >> 1) + ((ut >> 3) & 3)) & 3;
     const int vch = ut;  // V: channel
     // ---- fused append: the tree rows whose keys fall in this unit's range ----
     // (a1 for KV head h; thread ut = channel, warp = 32-channel group, the
@@ -769,16 +776,22 @@ __global__ void __launch_bounds__(kFused ? kThreads + 32 : kThreads, 1)
         const uint2 w01 = wv[0], w23 = wv[1], w45 = wv[2];
         const __half2 sc2 = *reinterpret_cast<const __half2*>(stage + kKTileCodeBytes + kj * 16 + kcb * 4);
         const uint32_t krow = su32(kdeq0) + b * kOperandBytes + kcb * 8192 + sw128_row(kj);
-        const __half2 s0 = __low2half2(sc2), s1 = __high2half2(sc2);
+        // group 2 kcb (words 0-2, chunks 0-3) and group 2 kcb + 1 (words 3-5,
+        // chunks 4-7); an odd block does the second group first
+        const bool odd = kcb & 1;
+        const uint32_t a0 = odd ? w23.y : w01.x, a1 = odd ? w45.x : w01.y, a2 = odd ? w45.y : w23.x;
+        const uint32_t b0 = odd ? w01.x : w23.y, b1 = odd ? w01.y : w45.x, b2 = odd ? w23.x : w45.y;
+        const __half2 sa = odd ? __high2half2(sc2) : __low2half2(sc2), sb = odd ? __low2half2(sc2) : __high2half2(sc2);
+        const int ca = odd ? 4 : 0;
         __half2 out[16];
-        decode_block_h2(w01.x, w01.y, w23.x, [&](int) { return s0; }, out);
+        decode_block_h2(a0, a1, a2, [&](int) { return sa; }, out);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
-          st_shared_v4(sw128_chunk(krow, q4), out[4 * q4], out[4 * q4 + 1], out[4 * q4 + 2], out[4 * q4 + 3]);
-        decode_block_h2(w23.y, w45.x, w45.y, [&](int) { return s1; }, out);
+          st_shared_v4(sw128_chunk(krow, ca + q4), out[4 * q4], out[4 * q4 + 1], out[4 * q4 + 2], out[4 * q4 + 3]);
+        decode_block_h2(b0, b1, b2, [&](int) { return sb; }, out);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
-          st_shared_v4(sw128_chunk(krow, 4 + q4), out[4 * q4], out[4 * q4 + 1], out[4 * q4 + 2], out[4 * q4 + 3]);
+          st_shared_v4(sw128_chunk(krow, (ca ^ 4) + q4), out[4 * q4], out[4 * q4 + 1], out[4 * q4 + 2], out[4 * q4 + 3]);
       }
       // ---- V: channel vch, 64 keys -> one 128-byte swizzled row of V^T ----
       if constexpr (kI4) {
