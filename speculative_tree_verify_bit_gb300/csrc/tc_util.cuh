@@ -99,8 +99,10 @@ __device__ __forceinline__ bool settle(uint64_t* b, uint32_t parity, uint32_t pr
 // what those CTAs wrote before their increments is visible afterwards; the
 // proxy fence then orders it before this thread's later bulk copies.  The
 // CTAs waited for must be resident (a cooperative launch).  False on timeout
-// (about 1 s; sets the CTA's abort flag) or when the CTA aborted.
-constexpr uint32_t kCountWaitLimit = 1u << 20;
+// (at most about 1.5 s: each poll is a trip to L2 and a 128 ns sleep; sets
+// the CTA's abort flag) or when the CTA aborted.  The short sleep keeps the
+// waiter within a fraction of a microsecond of the last increment.
+constexpr uint32_t kCountWaitLimit = 1u << 21;
 __device__ __forceinline__ bool wait_count(const uint32_t* c, uint32_t target, volatile int* abort_flag) {
   for (uint32_t it = 0; it < kCountWaitLimit; ++it) {
     uint32_t v;
@@ -110,7 +112,7 @@ __device__ __forceinline__ bool wait_count(const uint32_t* c, uint32_t target, v
       return true;
     }
     if ((it & 63) == 63 && *abort_flag) return false;
-    __nanosleep(1000);
+    __nanosleep(128);
   }
   *abort_flag = 1;
   return false;

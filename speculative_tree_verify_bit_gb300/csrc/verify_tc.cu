@@ -172,17 +172,31 @@ __device__ __noinline__ void epilogue_rows_staged(uint32_t lane_addr, uint8_t* s
 __device__ __noinline__ void fused_pack_tree_rows(const VerifyParams& p) {
   const int lane = threadIdx.x & 31;
   bool packed = false;
+  // Start this unit's rows (512 bytes of K and of V each) on their way to L2
+  // first: the packing loop loads them one 32-channel group at a time, each
+  // group after the previous group's stores, so every load would otherwise
+  // wait out a full trip to HBM.
+  for (int q = blockIdx.x; q < p.n_pairs; q += p.n_units) {
+    const int64_t row = (int64_t)q * kHeadDim;  // pair q = (sequence row, KV head)
+    if (lane < 4) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.k_tree + row + lane * 64));
+    else if (lane < 8) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.v_tree + row + (lane - 4) * 64));
+  }
   for (int q = blockIdx.x; q < p.n_pairs; q += p.n_units) {
     const int h2 = q % p.hkv, si = q / p.hkv, s2 = si / p.T;
     const int64_t pos = (int64_t)p.seq[s2].ctx + si % p.T;
     const int64_t row = ((int64_t)si * p.hkv + h2) * kHeadDim;
+    // all eight groups' values in flight at once (read-only loads), then
+    // the rolled packing loop over them
+    __half2 kv[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+      kv[g] = __halves2half2(__ldg(p.k_tree + row + g * 32 + lane), __ldg(p.v_tree + row + g * 32 + lane));
     uint8_t* hb = const_cast<uint8_t*>(
         head_block(p.seq[s2], p.pool, p.page_bytes, p.pool_pages, pos, h2, lane == 0 ? p.status : nullptr));
     if (hb) {
 #pragma unroll 1
       for (int g = 0; g < 8; ++g)
-        append_row_channel(__half2float(p.k_tree[row + g * 32 + lane]), __half2float(p.v_tree[row + g * 32 + lane]),
-                           hb, (int)(pos & (kPageTok - 1)), g * 32 + lane);
+        append_row_channel(__low2float(kv[g]), __high2float(kv[g]), hb, (int)(pos & (kPageTok - 1)), g * 32 + lane);
     }
     packed = true;
   }
