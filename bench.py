@@ -355,7 +355,7 @@ def measure_lookup(w: workloads.Workload, dev, reps: int = 50, min_len: int = 6,
     prop = torch.zeros((n, k), dtype=torch.int32, device=dev)
     mlen = torch.zeros(n, dtype=torch.int32, device=dev)
     mpos = torch.zeros(n, dtype=torch.int64, device=dev)
-    ws = torch.empty(stv.stv_lookup_workspace_bytes(n), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(stv.stv_lookup_workspace_bytes(n), dtype=torch.uint8, device=dev)  # left zero by each call
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     times = []
     for i in range(reps + 3):

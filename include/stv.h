@@ -444,8 +444,10 @@ int stv_prefill_attn_timeout_test(const stv_shape* shape, const stv_layer_cache*
  *  prop:      device int32 [n_seqs][k]: the proposal, zero beyond n_prop.
  *  match_len: device int32 [n_seqs]: L, or 0 when nothing matched.
  *  match_pos: device int64 [n_seqs]: p, or -1 when nothing matched.
- *  workspace: device, at least stv_lookup_workspace_bytes(n_seqs) bytes;
- *             caller-owned scratch, contents need not be preserved.
+ *  workspace: device, at least stv_lookup_workspace_bytes(n_seqs) bytes,
+ *             caller-owned, ZERO before the first call (e.g. allocated
+ *             zeroed); every call leaves the bytes it used zero again, so
+ *             the same workspace serves any later call without clearing.
  * Returns STV_ERR_INVALID_ARG for lengths, k or n_seqs out of range, null
  * pointers or a workspace too small (STV_ERR_WORKSPACE_TOO_SMALL).  The
  * result is unique, so it does not depend on timing.

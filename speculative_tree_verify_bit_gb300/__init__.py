@@ -386,7 +386,8 @@ def stv_lookup_draft(histories, min_len: int, max_len: int, k: int, n_prop, prop
                      stream=None):
     """Lookup drafting over each history (int32 CUDA tensors): the up to k
     tokens that followed the latest earlier occurrence of the longest suffix
-    of length max_len .. min_len (include/stv.h)."""
+    of length max_len .. min_len (include/stv.h).  The workspace must be zero
+    before its first use; each call leaves it zero."""
     import torch
 
     arr = (stv_history * len(histories))()

@@ -17,7 +17,9 @@
 // (plus max_len - 1 tokens to its left) in shared memory with coalesced
 // loads, reduces its chunk, and folds the result into the sequence's key
 // with a 64-bit atomicMax.  The last CTA of a sequence to finish (a done
-// counter; no CTA ever waits for another) writes the proposal.  It reads
+// counter; no CTA ever waits for another) writes the proposal and sets the
+// sequence's key and counter back to zero, so the workspace, zero before the
+// first call, is zero before every call (no clearing launch).  It reads
 // 4 bytes of history per token; at one request's history (a megabyte at 262K
 // tokens) the call is bound by launch and load latency rather than bandwidth.
 #include <stdint.h>
@@ -42,8 +44,8 @@ struct LookupParams {
   int32_t* prop;
   int32_t* match_len;
   int64_t* match_pos;
-  unsigned long long* key;  // per sequence, zero at launch
-  unsigned int* done;       // per sequence, zero at launch
+  unsigned long long* key;  // per sequence, zero at launch, left zero
+  unsigned int* done;       // per sequence, zero at launch, left zero
 };
 
 __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long x) {
@@ -111,6 +113,11 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const __grid_constant_
   const int64_t e = (int64_t)(key & 0xffffffffull);
   const int64_t avail = L ? n - 1 - e : 0;
   const int cnt = (int)(avail < p.k ? avail : p.k);
+  // every other CTA of this sequence has folded in its key and counted itself
+  if (tid == 0) {
+    p.key[s] = 0ull;
+    p.done[s] = 0u;
+  }
   for (int j = tid; j < p.k; j += kThreads) p.prop[(int64_t)s * p.k + j] = j < cnt ? h[e + 1 + j] : 0;
   if (tid == 0) {
     p.n_prop[s] = cnt;
@@ -161,7 +168,6 @@ extern "C" int stv_lookup_draft(const stv_history* hist, int n_seqs, int min_len
   p.key = static_cast<unsigned long long*>(workspace);
   p.done = reinterpret_cast<unsigned int*>(static_cast<unsigned long long*>(workspace) + n_seqs);
   cudaStream_t st = (cudaStream_t)stream;
-  if (cudaMemsetAsync(workspace, 0, need, st) != cudaSuccess) return STV_ERR_CUDA;
   lookup_kernel<<<ctas, kThreads, 0, st>>>(p);
   return cudaGetLastError() == cudaSuccess ? STV_OK : STV_ERR_CUDA;
 }

@@ -12,7 +12,7 @@ import workloads
 pytestmark = pytest.mark.gpu
 
 
-def gpu_lookup(histories, min_len=6, max_len=12, k=15):
+def gpu_lookup(histories, min_len=6, max_len=12, k=15, ws=None):
     dev = "cuda"
     n = len(histories)
     hs = [torch.as_tensor(np.asarray(h, np.int32), device=dev) for h in histories]
@@ -20,14 +20,16 @@ def gpu_lookup(histories, min_len=6, max_len=12, k=15):
     prop = torch.full((n, max(k, 1)), -7, dtype=torch.int32, device=dev)
     mlen = torch.full((n,), -7, dtype=torch.int32, device=dev)
     mpos = torch.full((n,), -7, dtype=torch.int64, device=dev)
-    ws = torch.empty(stv.stv_lookup_workspace_bytes(n), dtype=torch.uint8, device=dev)
+    if ws is None:
+        ws = torch.zeros(stv.stv_lookup_workspace_bytes(n), dtype=torch.uint8, device=dev)
     stv.stv_lookup_draft(hs, min_len, max_len, k, n_prop, prop, mlen, mpos, ws)
     torch.cuda.synchronize()
+    assert int(ws.count_nonzero().item()) == 0, "workspace not left zero"
     return n_prop.cpu().numpy(), prop.cpu().numpy(), mlen.cpu().numpy(), mpos.cpu().numpy()
 
 
-def assert_matches_oracle(histories, min_len=6, max_len=12, k=15):
-    n_prop, prop, mlen, mpos = gpu_lookup(histories, min_len, max_len, k)
+def assert_matches_oracle(histories, min_len=6, max_len=12, k=15, ws=None):
+    n_prop, prop, mlen, mpos = gpu_lookup(histories, min_len, max_len, k, ws)
     for s, h in enumerate(histories):
         want, wl, wp = oracle.lookup_draft(h, min_len, max_len, k)
         assert n_prop[s] == len(want), (s, len(h))
@@ -63,6 +65,17 @@ def test_ragged_and_long_workload_histories(gpu):
         w = workloads.WORKLOADS[name]
         for p_copy in (1.0, 0.0):
             assert_matches_oracle(workloads.lookup_histories(w, p_copy))
+
+
+def test_workspace_zeroed_once_serves_every_call(gpu):
+    """One workspace, zeroed once, for calls with 8, 1, 3 and 8 sequences
+    (the counters' offsets move with the count): each call leaves it zero and
+    matches the oracle."""
+    rng = np.random.default_rng(91)
+    ws = torch.zeros(stv.stv_lookup_workspace_bytes(8), dtype=torch.uint8, device=gpu)
+    for n in (8, 1, 3, 8):
+        hs = [rng.integers(0, 3, int(rng.integers(1, 9000))).astype(np.int32) for _ in range(n)]
+        assert_matches_oracle(hs, 2, 12, 15, ws=ws)
 
 
 def test_rejects_bad_arguments(gpu):
