@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const __grid_constant_
   __shared__ int32_t win[kChunk + kMaxLen];
   __shared__ int32_t suf[kMaxLen];  // suf[i] = h[n - 1 - i]
   __shared__ unsigned long long red[kThreads / 32];
+  __shared__ unsigned long long final_key;
   __shared__ int is_last;
   const int tid = threadIdx.x;
   int s = 0;
@@ -107,17 +108,21 @@ __global__ void __launch_bounds__(kThreads) lookup_kernel(const __grid_constant_
   if (!is_last) return;
 
   // ---- last CTA of sequence s: write the proposal ----
-  __threadfence();
-  const unsigned long long key = atomicAdd(p.key + s, 0ull);
+  // One thread reads the final key (every other CTA of this sequence has
+  // folded in its key and counted itself) and sets the key and the counter
+  // back to zero for the next call; the CTA reads the key from shared memory.
+  if (tid == 0) {
+    __threadfence();
+    final_key = atomicAdd(p.key + s, 0ull);
+    p.key[s] = 0ull;
+    p.done[s] = 0u;
+  }
+  __syncthreads();
+  const unsigned long long key = final_key;
   const int L = (int)(key >> 32);
   const int64_t e = (int64_t)(key & 0xffffffffull);
   const int64_t avail = L ? n - 1 - e : 0;
   const int cnt = (int)(avail < p.k ? avail : p.k);
-  // every other CTA of this sequence has folded in its key and counted itself
-  if (tid == 0) {
-    p.key[s] = 0ull;
-    p.done[s] = 0u;
-  }
   for (int j = tid; j < p.k; j += kThreads) p.prop[(int64_t)s * p.k + j] = j < cnt ? h[e + 1 + j] : 0;
   if (tid == 0) {
     p.n_prop[s] = cnt;
