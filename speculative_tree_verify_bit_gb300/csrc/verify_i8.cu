@@ -28,16 +28,19 @@
 //               straight into tensor memory.
 //   warps 1-2   idle.
 // Per 64-key tile:
-//   I_g[128 rows x 64 keys] = Q_g (TMEM) . C_g^T (shared), one group per
-//                             round (eight per tile), each round's dots in
-//                             one of two TMEM blocks of 64 columns (one
+//   I_g[128 rows x 64 keys] = Q_g (shared) . C_g^T (shared), two groups per
+//                             round (four per tile), each round's dots in
+//                             one of two TMEM blocks of 128 columns (one
 //                             block when T * G > 96)
 //   O^T[256 ch x NP rows]  += V^T (TMEM, two 128-channel halves) . P^T (shared)
 // The second is P.V with the operands swapped (M = the 256 channels, N = the
 // NP = ceil16(T*G) real rows), which keeps the accumulator small enough to
-// leave room for the per-group dots.  Tensor memory (512 columns): qi as
-// fp16 [0,128); the rounds' dot blocks from column 128; one V^T buffer of
-// 64 columns; O^T halves of NO = ceil32(T*G) columns at the end.
+// leave room for the per-group dots.  qi (fp16, the A operand of the dots)
+// sits in shared memory, so that tensor memory (512 columns) holds two dot
+// blocks of two groups each from column 0, one V^T buffer of 64 columns,
+// and the O^T halves of NO = ceil32(T*G) columns at the end: every round
+// is a hand-off between the MMA warp and the softmax warps, and two groups
+// per round halve their number.
 // Softmax is online in fp32 with a stale-maximum threshold: P uses a
 // reference maximum that is raised (rescaling O and l) only when a score
 // exceeds it by more than 2^8, so P <= 256 in fp16 and O rescales are rare.
@@ -50,24 +53,35 @@ namespace stv {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kKBuffers = 3;          // decoded K tiles in shared memory
+constexpr int kQBytes = 65536;        // qi as the A operand: 128 rows x 256 channels, fp16
+constexpr int kKBuffers = 2;          // decoded K tiles in shared memory
 constexpr int kOperandBytes = 32768;  // one fp16 K tile: 64 keys x 256 channels
 constexpr int kPBytes = 16384;        // one fp16 P tile: up to 128 rows x 64 keys
 constexpr int kCtlBytes = 2048;       // barriers, masks, rescale factors
-constexpr int kStages = 6;            // raw ring
+constexpr int kStages = 3;            // raw ring
 constexpr int kStageBytes = kKTileCodeBytes + kKTileScaleBytes + kVTileCodeBytes + kVTileScaleBytes;  // 14336
 // Per-(key, group) K scales handed from the unpack warps to the softmax
 // warps, as fp32, in rotating slots (one barrier per slot).  Unpacking tile
-// j waits for QK(j - 3) to finish, so the softmax warps have loaded most of
-// tile j - 3's rounds and are done with tile j - 4: slot j mod 4 is never
-// rewritten while it is read.
+// j waits for QK(j - 2) to finish, whose rounds reuse dot blocks that the
+// softmax warps released while reading tile j - 3's: they are done with
+// tile j - 4, so slot j mod 4 is never rewritten while it is read.
 constexpr int kSlots = 4;
 constexpr int kSlotFloats = kGroups * kTileTok;
-constexpr int kSmemBytes = 1024 /*align slack*/ + kKBuffers * kOperandBytes + 2 * kPBytes + kStages * kStageBytes +
-                           kCtlBytes + kSlots * kSlotFloats * 4;
+constexpr int kSmemBytes = 1024 /*align slack*/ + kQBytes + kKBuffers * kOperandBytes + 2 * kPBytes +
+                           kStages * kStageBytes + kCtlBytes + kSlots * kSlotFloats * 4;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr float kRescaleThreshold = 8.f;  // log2 units
-constexpr uint32_t kColQ = 0, kColS = 128, kTmemCols = 512;
+constexpr uint32_t kColS = 0, kTmemCols = 512;
+
+// D (TMEM) = A (shared-memory descriptor) x B (shared-memory descriptor) (+ D
+// when acc != 0), issued by one elected lane.
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, e;\n setp.ne.u32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
 
 struct Ctl {
   uint64_t raw_full[kStages], raw_empty[kStages];
@@ -121,8 +135,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_con
   // 1024-byte alignment of the operand tiles (the swizzle works on address bits).
   const uint32_t base_u32 = su32(smem_raw);
   uint8_t* smem = smem_raw + ((1024 - (base_u32 & 1023)) & 1023);
-  uint8_t* const kbuf0 = smem;                              // K tiles: kbuf0 + b * kOperandBytes
-  uint8_t* const pbuf0 = smem + kKBuffers * kOperandBytes;  // P tiles: pbuf0 + b * kPBytes
+  uint8_t* const qbuf0 = smem;                              // qi, the A operand of the dot MMAs
+  uint8_t* const kbuf0 = smem + kQBytes;                    // K tiles: kbuf0 + b * kOperandBytes
+  uint8_t* const pbuf0 = kbuf0 + kKBuffers * kOperandBytes;  // P tiles: pbuf0 + b * kPBytes
   uint8_t* const ring = pbuf0 + 2 * kPBytes;
   Ctl* ctl = reinterpret_cast<Ctl*>(ring + kStages * kStageBytes);
   float* const kscale = reinterpret_cast<float*>(ring + kStages * kStageBytes + kCtlBytes);
@@ -149,11 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_con
   // ---- tensor-memory plan (R <= 128 rows) ----
   const int NP = (R + 15) & ~15;  // N of the P.V product
   const int NO = (R + 31) & ~31;  // columns of one O^T half
-  // One group per QK round (eight rounds per tile), its dots in one of nsb
-  // TMEM blocks of 64 columns: two (the MMA of round k + 1 overlaps the
+  // Two groups per QK round (four rounds per tile), their dots in one of nsb
+  // TMEM blocks of 128 columns: two (the MMA of round k + 1 overlaps the
   // softmax warps' loads of round k) when the O^T halves leave room.
   const int nsb = NO <= 96 ? 2 : 1;
-  const uint32_t s_end = kColS + 64 * nsb;  // the V^T buffer: [s_end, s_end + 64)
+  const uint32_t s_end = kColS + 128 * nsb;  // the V^T buffer: [s_end, s_end + 64)
   const uint32_t colO = kTmemCols - 2 * NO;
 
   // ---- set-up ----
@@ -261,7 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_con
     const uint32_t tm = tmem;
     bool ok = waitw(&ctl->q_ready, 0, abort_flag);
     tc_after();
-    const uint64_t kdesc0 = desc_sw128(su32(kbuf0)), pdesc0 = desc_sw128(su32(pbuf0));
+    const uint64_t qdesc0 = desc_sw128(su32(qbuf0)), kdesc0 = desc_sw128(su32(kbuf0)),
+                   pdesc0 = desc_sw128(su32(pbuf0));
     const uint32_t idesc_qk = idesc_f16_f32(128, 64), idesc_pv = idesc_f16_f32(128, NP);
     uint32_t rnd = 0;  // QK rounds issued so far
     auto issue_qk = [&](int i) -> bool {
@@ -270,20 +286,25 @@ __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_con
                   abort_flag))
         return false;
       const uint64_t kd = kdesc0 + (uint64_t)(kb * (kOperandBytes >> 4));
-      for (int g = 0; g < kGroups; ++g) {
+      for (int rr = 0; rr < kGroups / 2; ++rr) {
         const int b = rnd % nsb;
         const uint32_t u = rnd / nsb;  // this block's use count
         if (u > 0 && !settle(&ctl->s_free[b], (u - 1) & 1, probe(&ctl->s_free[b], (u - 1) & 1), abort_flag))
           return false;
         tc_after();
-        // group g's 32 channels are K16 steps 2g and 2g + 1
+        // groups 2 rr and 2 rr + 1, each into its 64 columns of the block;
+        // group g's 32 channels are K16 steps 2g and 2g + 1 (qi: 16 KiB per
+        // 64-channel block, the K tile: 8 KiB)
 #pragma unroll
-        for (int t2 = 0; t2 < 2; ++t2) {
-          const int kk = 2 * g + t2;
-          mma_tmemA(tm + kColS + 64 * b, tm + kColQ + 8 * kk, kd + (uint64_t)((kk >> 2) * 512 + (kk & 3) * 2),
-                    idesc_qk, t2 > 0);
+        for (int gg = 0; gg < 2; ++gg) {
+#pragma unroll
+          for (int t2 = 0; t2 < 2; ++t2) {
+            const int kk = 2 * (2 * rr + gg) + t2;
+            mma_ss(tm + kColS + 128 * b + 64 * gg, qdesc0 + (uint64_t)((kk >> 2) * 1024 + (kk & 3) * 2),
+                   kd + (uint64_t)((kk >> 2) * 512 + (kk & 3) * 2), idesc_qk, t2 > 0);
+          }
         }
-        if (g == kGroups - 1) tc_commit(&ctl->kd_empty[kb]);
+        if (rr == kGroups / 2 - 1) tc_commit(&ctl->kd_empty[kb]);
         tc_commit(&ctl->s_full[b]);
         ++rnd;
       }
@@ -326,7 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_con
     const bool live = r < R;
     float c = kLog2e / 16.f;  // S c = sQ sum_g sK_g I_g / 16 in log2 units
     int node = 0;
-    // qi row (exact integers in fp16) -> TMEM columns [0, 128)
+    // qi row (exact integers in fp16) -> row r of the A operand in shared
+    // memory: four 64-channel blocks of 128 rows x 128 bytes, 128-byte swizzle
     {
       int64_t qrow = 0;
       if (live) {
@@ -346,10 +368,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_con
           for (int e = 0; e < 32; ++e)
             v[e] = h2u(__halves2half2(__int2half_rn(src[2 * e]), __int2half_rn(src[2 * e + 1])));
         }
-        tmem_st32(lane_addr + kColQ + 32 * chunk, v);
+        const uint32_t qrow_s = su32(qbuf0) + chunk * (kQBytes / 4) + sw128_row(r);
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8)
+          st_shared_v4(sw128_chunk(qrow_s, c8), v[4 * c8], v[4 * c8 + 1], v[4 * c8 + 2], v[4 * c8 + 3]);
       }
-      tmem_wait_st();
-      tc_before();
+      fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->q_ready);
     }
@@ -375,7 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_con
 #pragma unroll
         for (int e = 0; e < 64; ++e) sv[e] = 0u;  // fp32 zero
         const float* ksl = kscale + (i % kSlots) * kSlotFloats;
-        for (int g = 0; g < kGroups && !fail; ++g) {
+        // a round holds groups 2 rr and 2 rr + 1: four 32-key parts, taken
+        // in group order (S sums the groups in order 0..7)
+        for (int rr = 0; rr < kGroups / 2 && !fail; ++rr) {
           const int sb = rnd % nsb;
           if (!waitw(&ctl->s_full[sb], (rnd / nsb) & 1, abort_flag)) {
             fail = true;
@@ -383,11 +409,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_i8_kernel(const __grid_con
           }
           tc_after();
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
+          for (int part = 0; part < 4; ++part) {
+            const int g = 2 * rr + (part >> 1), half = part & 1;
             uint32_t t[32];
-            tmem_ld32(lane_addr + kColS + 64 * sb + 32 * half, t);
+            tmem_ld32(lane_addr + kColS + 128 * sb + 32 * part, t);
             tmem_wait_ld(t);
-            if (half == 1) {  // the round's last load: release the block
+            if (part == 3) {  // the round's last load: release the block
               tc_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(&ctl->s_free[sb]);
